@@ -1,0 +1,253 @@
+/*
+ * nvfp4moe.h — C ABI of the GB300 (sm_103a) NVFP4 MoE expert FFN library
+ * (libnvfp4moe.so).
+ *
+ * The forward pass of one mixture-of-experts expert FFN with NVFP4 (E2M1
+ * values, 16-element E4M3 block scales, fp32 global scales), as described by
+ * the "NVFP4 MegaMoE Debug Log" (Architecture Notes, "NVFP4 MoE Pipeline"):
+ *
+ *   1. moe_route_permute      group the T*k (token, choice) slots by expert
+ *   2. nvfp4_quantize_act     dynamic activation quantisation (stage_activation)
+ *   3-6. moe_nvfp4_forward    L1 grouped GEMM over [gate; up], SiLU(gate)*up,
+ *                             requantisation, L2 grouped GEMM, per-expert alpha
+ *   7. moe_unpermute_reduce   top-k weighted reduce back to token order
+ *
+ * plus two offline weight helpers (nvfp4_quantize_weights,
+ * moe_nvfp4_prepare_weights).
+ *
+ * Conventions (all entry points):
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *    stated otherwise.  The library never allocates or frees device memory,
+ *    never synchronises the host and keeps no state between calls except a
+ *    per-device cache of kernel attributes.
+ *  - Work is enqueued on `stream`; a call returns once its kernels are
+ *    enqueued.  Calls are stream-ordered and may be captured in a CUDA graph.
+ *  - The return value is an nvmoe_status.  Host-side argument checks run
+ *    before anything is enqueued; a nonzero status means nothing was enqueued
+ *    (except NVMOE_ERR_CUDA, returned when a launch fails).  No C++ exception
+ *    crosses the ABI.
+ *  - Faults detected on the device (a wait that exceeded its time limit, an
+ *    expert id out of range) do not trap: the kernel records a status code in
+ *    a caller-visible status word and returns (see nvmoe_read_status).
+ *  - Pointers must be 16-byte aligned.
+ *
+ * Slot layout.  Routing produces a grouped "row" layout: expert e owns rows
+ * [expert_offsets[e], expert_offsets[e] + expert_counts[e]), and every
+ * expert_offsets[e] is a multiple of NVMOE_TILE_ROWS (128); rows between an
+ * expert's last slot and the next multiple of 128 are padding.  Within an
+ * expert, slots are in ascending flat order t*k + j (stable counting sort).
+ *
+ * Block-scale staging ("MMA layout").  Block scales consumed by the tensor
+ * cores are stored in 512-byte atoms covering 128 rows x 64 elements
+ * (4 scale bytes per row).  For a matrix with R rows (R padded up to a
+ * multiple of 128) and K elements per row (K padded up to a multiple of 256,
+ * K_pad), the scale byte of (row r, 16-element group g) lives at
+ *   ((r / 128) * (K_pad / 64) + g / 4) * 512
+ *     + (r % 32) * 16 + ((r % 128) / 32) * 4 + (g % 4).
+ * nvfp4_sf_mma_bytes() gives the buffer size.  Padding bytes are unspecified.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVMOE_TILE_ROWS 128
+
+typedef enum {
+  NVMOE_OK = 0,
+  NVMOE_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum */
+  NVMOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set      */
+  NVMOE_ERR_MISALIGNED = 3,         /* pointer not 16-byte aligned           */
+  NVMOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  NVMOE_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed     */
+  NVMOE_ERR_TIMEOUT = 6,            /* device: a bounded wait ran out        */
+  NVMOE_ERR_DEVICE_BAD_INDEX = 7    /* device: expert id out of [0, E)       */
+} nvmoe_status;
+
+/* Element types of activation / output buffers. */
+typedef enum { NVMOE_BF16 = 0, NVMOE_F32 = 1 } nvmoe_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvmoe_status_str(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int nvmoe_version(void);
+
+/* Read (and optionally clear) the device status word that a workspace
+ * carries at its start.  Synchronises `stream`.  `status_out` is a HOST
+ * pointer.  Every workspace-taking call writes only nonzero codes there; a
+ * fresh workspace must start zeroed (nvmoe_clear_status). */
+int nvmoe_read_status(const void* workspace, cudaStream_t stream, int* status_out);
+int nvmoe_clear_status(void* workspace, cudaStream_t stream);
+
+/* Size in bytes of a staged (MMA layout) block-scale buffer for `rows` rows
+ * of `cols` elements. */
+size_t nvfp4_sf_mma_bytes(int64_t rows, int64_t cols);
+
+/* ---------------------------------------------------------------- step 1 --
+ * moe_route_permute — per-expert histogram, prefix sum and stable slot
+ * assignment of the top-k routing choice ("NVFP4 MegaMoE Debug Log":
+ * pipeline trace "slots=", later log "L2 slot_token"; the scatter with routing
+ * weights of the NVFP4 MoE Pipeline needs the inverse map slot_of).
+ *
+ *   topk_ids        int32 [T, k], row-major; each entry in [0, E).  An entry
+ *                   outside that range sets NVMOE_ERR_DEVICE_BAD_INDEX in the
+ *                   workspace status word and is dropped.
+ *   expert_offsets  int32 [E + 1] out: first row of each expert (multiples of
+ *                   128); expert_offsets[E] = number of rows in use.
+ *   expert_counts   int32 [E] out: slots per expert.
+ *   row_token       int32 [moe_route_rows_bound(T,k,E)] out: token of each
+ *                   row, -1 on padding rows and on rows past expert_offsets[E].
+ *   slot_of         int32 [T * k] out: row of (token t, choice j) at t*k + j.
+ * Limits: 1 <= k <= 32, 1 <= E <= 256, T*k < 2^31.  T = 0 is valid (no-op
+ * apart from zero offsets/counts and -1 row tokens).
+ */
+int64_t moe_route_rows_bound(int64_t T, int k, int E);
+size_t moe_route_workspace_size(int64_t T, int k, int E);
+int moe_route_permute(const int32_t* topk_ids, int64_t T, int k, int E,
+                      int32_t* expert_offsets, int32_t* expert_counts,
+                      int32_t* row_token, int32_t* slot_of,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- step 2 --
+ * nvfp4_quantize_act — dynamic NVFP4 quantisation of activations
+ * ("NVFP4 MegaMoE Debug Log", Hypotheses §6 steps 1-5 and §5 packing; commit
+ * message "Three bugs fixed" on src).  In IEEE fp32, round-to-nearest-even:
+ *   amax = max |x| over the whole input;  gs = amax / 2688  (1.0 if amax = 0)
+ *   per 16-element block along a row:  b = max |x_i|,
+ *     sf = E4M3_satfinite(b / (6 * gs)),  d = dec(sf) * gs,
+ *     nibble_i = E2M1_satfinite(|x_i| / d) with bit 3 = sign bit of x_i
+ *     (all nibbles 0 when d == 0)
+ *   element 2j goes to the low nibble of byte j, 2j+1 to the high nibble.
+ *
+ *   x            [rows, cols] row-major, x_dtype = NVMOE_BF16 or NVMOE_F32.
+ *   row_dst      optional int32 [rows * fanout]: input row r is written to
+ *                output rows row_dst[r*fanout + j], j < fanout (use the
+ *                slot_of of moe_route_permute with fanout = k to quantise
+ *                straight into the grouped slot layout).  NULL: row r -> r.
+ *   out_rows     number of output rows (>= rows when row_dst is NULL).
+ *   q            uint8 [out_rows, cols/2] packed nibbles.
+ *   sf_rowmajor  optional uint8 [out_rows, cols/16] scale bytes, row-major.
+ *   sf_mma       optional staged scales, nvfp4_sf_mma_bytes(out_rows, cols).
+ *   gs_out       float [1]: gs.
+ * Output rows not written by any input row are left untouched.
+ * Limits: cols % 64 == 0, 1 <= fanout <= 32.  rows = 0 writes gs = 1.
+ */
+size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t cols);
+int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                       const int32_t* row_dst, int fanout, int64_t out_rows,
+                       uint8_t* q, uint8_t* sf_rowmajor, uint8_t* sf_mma,
+                       float* gs_out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* ------------------------------------------------------ offline weights --
+ * nvfp4_quantize_weights — NVFP4 quantisation of fp32 expert weights into
+ * the checkpoint layout ("NVFP4 MegaMoE Debug Log", Hypotheses §6 steps 1-5
+ * and §2 shapes): per expert e, gs[e] = amax(W_e) / 2688; 16-element blocks
+ * run along K for each output column n; same arithmetic as step 2.
+ *   w    float [E, K, N] row-major (math layout, K = reduction dim)
+ *   q    uint8 [E, K/2, N]: byte (j, n) = element (2j, n) low, (2j+1, n) high
+ *   sf   uint8 [E, K/16, N]
+ *   gs   float [E]
+ * Limits: K % 64 == 0, N >= 1.
+ */
+size_t nvfp4_quantize_weights_workspace_size(int E, int K, int N);
+int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q,
+                           uint8_t* sf, float* gs, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/* moe_nvfp4_prepare_weights — checkpoint layout -> tensor-core layout (the
+ * B-operand byte transpose of "NVFP4 MegaMoE Debug Log", Hypotheses §8 and the
+ * later log's "B ColumnMajor" point; scale staging replaces the SF remap of
+ * the commit messages on src).  Nibble pairs stay along K.
+ *   q_ckpt  uint8 [E, K/2, N],  sf_ckpt uint8 [E, K/16, N]
+ *   q_out   uint8 [E, N, K/2]  (K-major rows of the B operand)
+ *   sf_out  staged scales of the [E*N, K] matrix: nvfp4_sf_mma_bytes(E*N, K)
+ * Limits: K % 64 == 0, N % 128 == 0.
+ */
+int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt,
+                              int E, int K, int N, uint8_t* q_out,
+                              uint8_t* sf_out, cudaStream_t stream);
+
+/* ------------------------------------------------------------ steps 3-6 --
+ * Prepared expert weights (all device pointers):
+ *   w1     uint8 [E, 2I, H/2]  L1 [gate; up] rows: gate = rows [0, I),
+ *          up = rows [I, 2I) of each expert (plain concatenation, commit
+ *          message on the removed 2-CTA interleave)
+ *   w1_sf  staged, nvfp4_sf_mma_bytes(E*2I, H);  gs_w1 float [E]
+ *   w2     uint8 [E, H, I/2];  w2_sf staged, nvfp4_sf_mma_bytes(E*H, I);
+ *   gs_w2  float [E]
+ */
+typedef struct {
+  int E, H, I;
+  const uint8_t* w1;
+  const uint8_t* w1_sf;
+  const float* gs_w1;
+  const uint8_t* w2;
+  const uint8_t* w2_sf;
+  const float* gs_w2;
+} nvmoe_weights;
+
+/* Optional outputs of intermediate results (any member may be NULL).
+ *   l1_out   float [rows, 2I]: alpha-scaled L1 output, [gate | up]
+ *   h        float [rows, I]:  SiLU(gate) * up (fp32)
+ *   hq       uint8 [rows, I/2]; hsf_mma staged nvfp4_sf_mma_bytes(rows, I)
+ *   gs_h     float [1]
+ * rows = moe_route_rows_bound(T, k, E); padding rows are unspecified.
+ * When h / hq / hsf_mma / gs_h are given they replace the workspace buffers
+ * of the same name (no extra traffic); l1_out costs one extra store. */
+typedef struct {
+  float* l1_out;
+  float* h;
+  uint8_t* hq;
+  uint8_t* hsf_mma;
+  float* gs_h;
+} nvmoe_taps;
+
+/* moe_nvfp4_forward — the expert FFN on grouped slots ("NVFP4 MegaMoE Debug
+ * Log", NVFP4 MoE Pipeline; Hypotheses §3 for alpha):
+ *   l1[r, :]  = (gs_x * gs_w1[e]) * sum_k dec(xq) dec(xsf) dec(w1) dec(w1_sf)
+ *   h[r, c]   = silu(l1[r, c]) * l1[r, I + c]          (fp32)
+ *   hq, hsf, gs_h = step-2 quantisation of h over all valid rows
+ *   out[r, :] = (gs_h * gs_w2[e]) * sum_k dec(hq) dec(hsf) dec(w2) dec(w2_sf)
+ * Alpha is applied to the fp32 accumulator, never folded into block scales.
+ *   xq        uint8 [rows, H/2] activations in the grouped slot layout
+ *   xsf_mma   staged scales of xq: nvfp4_sf_mma_bytes(rows, H)
+ *   gs_x      float [1]
+ *   expert_offsets, expert_counts, row_token: from moe_route_permute
+ *   slot_out  float [rows, H]  (padding rows unspecified)
+ * rows = moe_route_rows_bound(T, k, E).
+ * Limits: H % 256 == 0, I % 128 == 0, E <= 256.
+ */
+size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I);
+int moe_nvfp4_forward(const nvmoe_weights* weights, const uint8_t* xq,
+                      const uint8_t* xsf_mma, const float* gs_x,
+                      const int32_t* expert_offsets, const int32_t* expert_counts,
+                      const int32_t* row_token, int64_t T, int k,
+                      float* slot_out, const nvmoe_taps* taps,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- step 7 --
+ * moe_unpermute_reduce — "scatter with routing weights" of the NVFP4 MoE
+ * Pipeline, written as a deterministic gather:
+ *   y[t, :] = sum_{j = 0..k-1} topk_w[t, j] * slot_out[slot_of[t*k + j], :]
+ * accumulated in fp32 in ascending j, stored once as y_dtype (bf16 rounds to
+ * nearest even).
+ *   slot_out float [rows, H];  slot_of int32 [T*k];  topk_w float [T, k]
+ *   y        [T, H] of y_dtype (NVMOE_BF16 or NVMOE_F32)
+ * Limits: H % 8 == 0, 1 <= k <= 32.
+ */
+int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of,
+                         const float* topk_w, int64_t T, int k, int64_t H,
+                         void* y, int y_dtype, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,315 @@
+"""Thin ctypes binding of libnvfp4moe.so (argument marshalling only).
+
+Every computation runs in the library's CUDA kernels; this module allocates
+device buffers with PyTorch, passes raw pointers and the current CUDA stream,
+and turns nonzero status codes into exceptions.  There is no fallback: if
+the library is missing or was not built, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libnvfp4moe.so")
+
+BF16, F32 = 0, 1
+TILE_ROWS = 128
+
+_lib = None
+
+
+class NvmoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().nvmoe_status_str(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+                ("w1", ctypes.c_void_p), ("w1_sf", ctypes.c_void_p), ("gs_w1", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("gs_w2", ctypes.c_void_p)]
+
+
+class Taps(ctypes.Structure):
+    _fields_ = [("l1_out", ctypes.c_void_p), ("h", ctypes.c_void_p), ("hq", ctypes.c_void_p),
+                ("hsf_mma", ctypes.c_void_p), ("gs_h", ctypes.c_void_p)]
+
+
+# name -> (restype, argtypes)
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "nvmoe_status_str": (ctypes.c_char_p, [_I]),
+    "nvmoe_version": (_I, []),
+    "nvmoe_read_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
+    "nvmoe_clear_status": (_I, [_P, _P]),
+    "nvfp4_sf_mma_bytes": (_SZ, [_I64, _I64]),
+    "moe_route_rows_bound": (_I64, [_I64, _I, _I]),
+    "moe_route_workspace_size": (_SZ, [_I64, _I, _I]),
+    "moe_route_permute": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_quantize_workspace_size": (_SZ, [_I64, _I64]),
+    "nvfp4_quantize_act": (_I, [_P, _I, _I64, _I64, _P, _I, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_quantize_weights_workspace_size": (_SZ, [_I, _I, _I]),
+    "nvfp4_quantize_weights": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_nvfp4_prepare_weights": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_nvfp4_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
+    "moe_nvfp4_forward": (_I, [ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _I64, _I, _P,
+                               ctypes.POINTER(Taps), _P, _SZ, _P]),
+    "moe_unpermute_reduce": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _I, _P]),
+}
+
+
+def lib():
+    """Load libnvfp4moe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() first")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise NvmoeError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def sf_mma_bytes(rows: int, cols: int) -> int:
+    return int(lib().nvfp4_sf_mma_bytes(rows, cols))
+
+
+def rows_bound(T: int, k: int, E: int) -> int:
+    return int(lib().moe_route_rows_bound(T, k, E))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    return ws
+
+
+def read_status(ws: torch.Tensor, stream=None) -> int:
+    out = ctypes.c_int(0)
+    _check("nvmoe_read_status", lib().nvmoe_read_status(_ptr(ws), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+# ------------------------------------------------------------------ step 1 --
+@dataclass
+class Route:
+    expert_offsets: torch.Tensor   # int32 [E+1]
+    expert_counts: torch.Tensor    # int32 [E]
+    row_token: torch.Tensor        # int32 [rows]
+    slot_of: torch.Tensor          # int32 [T*k]
+    rows: int                      # rows_bound
+    T: int
+    k: int
+    E: int
+
+
+def route_permute(topk_ids: torch.Tensor, E: int, ws: Optional[torch.Tensor] = None,
+                  out: Optional[Route] = None, stream=None) -> Route:
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    rows = rows_bound(T, k, E)
+    if out is None:
+        out = Route(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                    torch.empty(E, dtype=torch.int32, device=dev),
+                    torch.empty(max(rows, 1), dtype=torch.int32, device=dev),
+                    torch.empty(max(T * k, 1), dtype=torch.int32, device=dev), rows, T, k, E)
+    need = int(lib().moe_route_workspace_size(T, k, E))
+    if ws is None:
+        ws = _workspace(need, dev)
+    _check("moe_route_permute", lib().moe_route_permute(
+        _ptr(topk_ids), T, k, E, _ptr(out.expert_offsets), _ptr(out.expert_counts),
+        _ptr(out.row_token), _ptr(out.slot_of), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ step 2 --
+def quantize_act(x: torch.Tensor, row_dst: Optional[torch.Tensor] = None, fanout: int = 1,
+                 out_rows: Optional[int] = None, rowmajor_sf: bool = True, mma_sf: bool = True,
+                 ws: Optional[torch.Tensor] = None, out=None, stream=None):
+    """Returns (q [out_rows, cols/2] u8, sf_row [out_rows, cols/16] u8 or None,
+    sf_mma (staged) u8 or None, gs [1] f32)."""
+    assert x.dim() == 2 and x.is_contiguous()
+    rows, cols = x.shape
+    dtype = {torch.bfloat16: BF16, torch.float32: F32}[x.dtype]
+    if out_rows is None:
+        out_rows = rows
+    dev = x.device
+    if out is None:
+        q = torch.empty((out_rows, cols // 2), dtype=torch.uint8, device=dev)
+        sf_row = torch.empty((out_rows, cols // 16), dtype=torch.uint8, device=dev) if rowmajor_sf else None
+        sf_mma = torch.zeros(sf_mma_bytes(out_rows, cols), dtype=torch.uint8, device=dev) if mma_sf else None
+        gs = torch.empty(1, dtype=torch.float32, device=dev)
+    else:
+        q, sf_row, sf_mma, gs = out
+    if ws is None:
+        ws = _workspace(lib().nvfp4_quantize_workspace_size(rows, cols), dev)
+    _check("nvfp4_quantize_act", lib().nvfp4_quantize_act(
+        _ptr(x), dtype, rows, cols, _ptr(row_dst), fanout, out_rows, _ptr(q), _ptr(sf_row),
+        _ptr(sf_mma), _ptr(gs), _ptr(ws), ws.numel(), _stream(stream)))
+    return q, sf_row, sf_mma, gs
+
+
+# ---------------------------------------------------------------- weights --
+def quantize_weights(w: torch.Tensor, stream=None):
+    """fp32 [E, K, N] -> checkpoint (q [E, K/2, N], sf [E, K/16, N], gs [E])."""
+    E, K, N = w.shape
+    dev = w.device
+    q = torch.empty((E, K // 2, N), dtype=torch.uint8, device=dev)
+    sf = torch.empty((E, K // 16, N), dtype=torch.uint8, device=dev)
+    gs = torch.empty(E, dtype=torch.float32, device=dev)
+    ws = _workspace(lib().nvfp4_quantize_weights_workspace_size(E, K, N), dev)
+    _check("nvfp4_quantize_weights", lib().nvfp4_quantize_weights(
+        _ptr(w), E, K, N, _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws), ws.numel(), _stream(stream)))
+    return q, sf, gs
+
+
+def prepare_weights(q_ckpt: torch.Tensor, sf_ckpt: torch.Tensor, stream=None):
+    """Checkpoint (E, K/2, N) + (E, K/16, N) -> (q [E, N, K/2], staged sf)."""
+    E, K2, N = q_ckpt.shape
+    K = 2 * K2
+    dev = q_ckpt.device
+    q = torch.empty((E, N, K2), dtype=torch.uint8, device=dev)
+    sf = torch.zeros(sf_mma_bytes(E * N, K), dtype=torch.uint8, device=dev)
+    _check("moe_nvfp4_prepare_weights", lib().moe_nvfp4_prepare_weights(
+        _ptr(q_ckpt), _ptr(sf_ckpt), E, K, N, _ptr(q), _ptr(sf), _stream(stream)))
+    return q, sf
+
+
+@dataclass
+class PreparedWeights:
+    E: int
+    H: int
+    I: int
+    w1: torch.Tensor
+    w1_sf: torch.Tensor
+    gs_w1: torch.Tensor
+    w2: torch.Tensor
+    w2_sf: torch.Tensor
+    gs_w2: torch.Tensor
+
+    def struct(self) -> Weights:
+        return Weights(self.E, self.H, self.I, _ptr(self.w1), _ptr(self.w1_sf), _ptr(self.gs_w1),
+                       _ptr(self.w2), _ptr(self.w2_sf), _ptr(self.gs_w2))
+
+    @staticmethod
+    def from_checkpoint(w1q, w1sf, gs1, w2q, w2sf, gs2) -> "PreparedWeights":
+        """w1q (E, H/2, 2I), w1sf (E, H/16, 2I), w2q (E, I/2, H), w2sf (E, I/16, H)."""
+        E, H2, N1 = w1q.shape
+        q1, s1 = prepare_weights(w1q, w1sf)
+        q2, s2 = prepare_weights(w2q, w2sf)
+        return PreparedWeights(E, 2 * H2, N1 // 2, q1, s1, gs1.contiguous(), q2, s2,
+                               gs2.contiguous())
+
+
+# ------------------------------------------------------------- steps 3-6 --
+def forward_workspace_bytes(T: int, k: int, E: int, H: int, I: int) -> int:
+    return int(lib().moe_nvfp4_workspace_size(T, k, E, H, I))
+
+
+def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Tensor,
+                  gs_x: torch.Tensor, route: Route, slot_out: Optional[torch.Tensor] = None,
+                  taps: Optional[dict] = None, ws: Optional[torch.Tensor] = None, stream=None):
+    dev = xq.device
+    if slot_out is None:
+        slot_out = torch.empty((route.rows, weights.H), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = _workspace(forward_workspace_bytes(route.T, route.k, weights.E, weights.H,
+                                                weights.I), dev)
+    t = None
+    if taps:
+        t = Taps(_ptr(taps.get("l1_out")), _ptr(taps.get("h")), _ptr(taps.get("hq")),
+                 _ptr(taps.get("hsf_mma")), _ptr(taps.get("gs_h")))
+    wst = weights.struct()
+    _check("moe_nvfp4_forward", lib().moe_nvfp4_forward(
+        ctypes.byref(wst), _ptr(xq), _ptr(xsf_mma), _ptr(gs_x), _ptr(route.expert_offsets),
+        _ptr(route.expert_counts), _ptr(route.row_token), route.T, route.k, _ptr(slot_out),
+        ctypes.byref(t) if t is not None else None, _ptr(ws), ws.numel(), _stream(stream)))
+    return slot_out
+
+
+# ------------------------------------------------------------------ step 7 --
+def unpermute_reduce(slot_out: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor,
+                     out_dtype=torch.bfloat16, y: Optional[torch.Tensor] = None, stream=None):
+    T, k = topk_w.shape
+    H = slot_out.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=out_dtype, device=slot_out.device)
+    code = {torch.bfloat16: BF16, torch.float32: F32}[y.dtype]
+    _check("moe_unpermute_reduce", lib().moe_unpermute_reduce(
+        _ptr(slot_out), _ptr(slot_of), _ptr(topk_w), T, k, H, _ptr(y), code, _stream(stream)))
+    return y
+
+
+# -------------------------------------------------------- whole forward --
+class MoELayer:
+    """The four calls of one forward pass on preallocated buffers.
+
+    ``forward(x, topk_ids, topk_w)`` runs route -> quantise (straight into
+    the grouped slot layout) -> L1 / SiLU*up / requantise / L2 -> reduce on
+    the current stream, with every buffer reused between calls (so it can be
+    captured in a CUDA graph).
+    """
+
+    def __init__(self, weights: PreparedWeights, T: int, k: int, device="cuda",
+                 out_dtype=torch.bfloat16):
+        self.w = weights
+        self.T, self.k = T, k
+        E, H, I = weights.E, weights.H, weights.I
+        dev = torch.device(device)
+        self.rows = rows_bound(T, k, E)
+        self.route = Route(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                           torch.empty(E, dtype=torch.int32, device=dev),
+                           torch.empty(max(self.rows, 1), dtype=torch.int32, device=dev),
+                           torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+                           self.rows, T, k, E)
+        self.ws_route = _workspace(lib().moe_route_workspace_size(T, k, E), dev)
+        self.ws_quant = _workspace(lib().nvfp4_quantize_workspace_size(T, H), dev)
+        self.ws_fwd = _workspace(forward_workspace_bytes(T, k, E, H, I), dev)
+        self.xq = torch.zeros((max(self.rows, 1), H // 2), dtype=torch.uint8, device=dev)
+        self.xsf = torch.zeros(max(sf_mma_bytes(self.rows, H), 16), dtype=torch.uint8, device=dev)
+        self.gs_x = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.slot_out = torch.zeros((max(self.rows, 1), H), dtype=torch.float32, device=dev)
+        self.y = torch.empty((T, H), dtype=out_dtype, device=dev)
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
+                taps: Optional[dict] = None, stream=None) -> torch.Tensor:
+        route_permute(topk_ids, self.w.E, ws=self.ws_route, out=self.route, stream=stream)
+        quantize_act(x, row_dst=self.route.slot_of, fanout=self.k, out_rows=self.rows,
+                     ws=self.ws_quant, out=(self.xq, None, self.xsf, self.gs_x), stream=stream)
+        nvfp4_forward(self.w, self.xq, self.xsf, self.gs_x, self.route, slot_out=self.slot_out,
+                      taps=taps, ws=self.ws_fwd, stream=stream)
+        unpermute_reduce(self.slot_out, self.route.slot_of, topk_w, y=self.y, stream=stream)
+        return self.y
+
+    def status(self) -> int:
+        for ws in (self.ws_route, self.ws_quant, self.ws_fwd):
+            s = read_status(ws)
+            if s:
+                return s
+        return 0

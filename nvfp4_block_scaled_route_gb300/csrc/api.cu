@@ -1,0 +1,356 @@
+// C-ABI entry points of libnvfp4moe.so (declared in include/nvfp4moe.h):
+// argument checks, workspace carving, TMA descriptor encoding and kernel
+// launches.  No allocation, no host synchronisation on the compute calls.
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nvfp4moe.h"
+#include "internal.h"
+
+using namespace nvmoe;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;   // every workspace starts with the status word
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- cuTensorMapEncodeTiled through the runtime's driver entry point ----
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 tensor [rows, row_bytes], box 128 x 128 bytes, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t row_bytes, int64_t rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? NVMOE_OK : NVMOE_ERR_CUDA; }
+
+// Workspace carving helper.
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t bytes) {
+    T* p = reinterpret_cast<T*>(base == nullptr ? nullptr : base + off);
+    off += align_up(bytes);
+    return p;
+  }
+};
+
+int64_t rows_bound(int64_t T, int k, int E) {
+  const int64_t S = T * k;
+  const int64_t pad = (S < E ? S : E) * (kTileRows - 1);
+  return round_up(S + pad, kTileRows);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvmoe_status_str(int s) {
+  switch (s) {
+    case NVMOE_OK: return "ok";
+    case NVMOE_ERR_INVALID_ARG: return "invalid argument";
+    case NVMOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case NVMOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case NVMOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case NVMOE_ERR_CUDA: return "CUDA error";
+    case NVMOE_ERR_TIMEOUT: return "device wait timed out";
+    case NVMOE_ERR_DEVICE_BAD_INDEX: return "expert id out of range";
+    default: return "unknown status";
+  }
+}
+
+int nvmoe_version(void) { return 100; }
+
+int nvmoe_read_status(const void* ws, cudaStream_t stream, int* out) {
+  if (ws == nullptr || out == nullptr) return NVMOE_ERR_INVALID_ARG;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  *out = v;
+  return NVMOE_OK;
+}
+
+int nvmoe_clear_status(void* ws, cudaStream_t stream) {
+  if (ws == nullptr) return NVMOE_ERR_INVALID_ARG;
+  return status_of(cudaMemsetAsync(ws, 0, kStatusBytes, stream));
+}
+
+size_t nvfp4_sf_mma_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return sf_mma_bytes(rows, cols);
+}
+
+// ------------------------------------------------------------- route ----
+int64_t moe_route_rows_bound(int64_t T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return rows_bound(T, k, E);
+}
+
+size_t moe_route_workspace_size(int64_t T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  const int64_t S = T * k;
+  const int64_t chunks = S > 0 ? ceil_div(S, route_chunk_elems()) : 1;
+  return kStatusBytes + align_up(static_cast<size_t>(chunks) * E * sizeof(int32_t));
+}
+
+int moe_route_permute(const int32_t* topk_ids, int64_t T, int k, int E, int32_t* expert_offsets,
+                      int32_t* expert_counts, int32_t* row_token, int32_t* slot_of, void* ws,
+                      size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts) return NVMOE_ERR_INVALID_ARG;
+  if (T * k >= (int64_t(1) << 31)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (expert_offsets == nullptr || expert_counts == nullptr || ws == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (T > 0 && (topk_ids == nullptr || row_token == nullptr || slot_of == nullptr))
+    return NVMOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_route_workspace_size(T, k, E)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t S = T * k;
+  const int n_chunks = static_cast<int>(S > 0 ? ceil_div(S, route_chunk_elems()) : 1);
+  Carve c{static_cast<uint8_t*>(ws)};
+  int* status = c.take<int>(kStatusBytes);
+  int32_t* chunk_counts = c.take<int32_t>(static_cast<size_t>(n_chunks) * E * sizeof(int32_t));
+  return status_of(launch_route(topk_ids, T, k, E, expert_offsets, expert_counts, row_token,
+                                rows_bound(T, k, E), slot_of, chunk_counts, n_chunks, status,
+                                stream));
+}
+
+// --------------------------------------------------------- quantiser ----
+size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t cols) {
+  (void)rows;
+  (void)cols;
+  return kStatusBytes + align_up(kQuantMaxPartials * sizeof(float));
+}
+
+int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                       const int32_t* row_dst, int fanout, int64_t out_rows, uint8_t* q,
+                       uint8_t* sf_rowmajor, uint8_t* sf_mma, float* gs_out, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (rows < 0 || cols <= 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
+  if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (cols % 64 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (fanout < 1 || fanout > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  if (row_dst == nullptr && (fanout != 1 || out_rows < rows)) return NVMOE_ERR_INVALID_ARG;
+  if (gs_out == nullptr || ws == nullptr) return NVMOE_ERR_INVALID_ARG;
+  if (rows > 0 && (x == nullptr || q == nullptr)) return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf_mma) || !aligned16(ws))
+    return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < nvfp4_quantize_workspace_size(rows, cols)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  Carve c{static_cast<uint8_t*>(ws)};
+  c.take<int>(kStatusBytes);
+  float* partial = c.take<float>(kQuantMaxPartials * sizeof(float));
+  const int64_t n = rows * cols;
+  const int parts = quant_amax_blocks(n);
+  cudaError_t e = launch_quant_amax(x, x_dtype, n, partial, parts, stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  return status_of(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr, partial,
+                                     parts, q, sf_rowmajor, sf_mma, gs_out, stream));
+}
+
+// ----------------------------------------------------------- weights ----
+size_t nvfp4_quantize_weights_workspace_size(int E, int K, int N) {
+  (void)K;
+  (void)N;
+  if (E < 1) return 0;
+  return kStatusBytes + align_up(static_cast<size_t>(E) * 64 * sizeof(float));
+}
+
+int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q, uint8_t* sf,
+                           float* gs, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (E < 1 || K < 1 || N < 1 || w == nullptr || q == nullptr || sf == nullptr ||
+      gs == nullptr || ws == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (K % 64 != 0 || E > 65535) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w) || !aligned16(ws)) return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < nvfp4_quantize_weights_workspace_size(E, K, N))
+    return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  Carve c{static_cast<uint8_t*>(ws)};
+  c.take<int>(kStatusBytes);
+  float* partial = c.take<float>(static_cast<size_t>(E) * 64 * sizeof(float));
+  cudaError_t e = launch_weight_amax(w, E, static_cast<int64_t>(K) * N, partial, 64, stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  return status_of(launch_weight_quant(w, E, K, N, partial, 64, q, sf, gs, stream));
+}
+
+int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int E, int K, int N,
+                              uint8_t* q_out, uint8_t* sf_out, cudaStream_t stream) {
+  if (E < 1 || K < 1 || N < 1 || q_ckpt == nullptr || sf_ckpt == nullptr ||
+      q_out == nullptr || sf_out == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % kTileRows != 0 || E > 65535) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  return status_of(launch_prepare_weights(q_ckpt, sf_ckpt, E, K, N, q_out, sf_out, stream));
+}
+
+// ----------------------------------------------------------- forward ----
+static size_t forward_layout(int64_t T, int k, int E, int H, int I, Carve* c, float** h,
+                             uint8_t** hq, uint8_t** hsf, float** gs_h, float** partial,
+                             int** status) {
+  const int64_t rows = rows_bound(T, k, E);
+  *status = c->take<int>(kStatusBytes);
+  *h = c->take<float>(static_cast<size_t>(rows) * I * sizeof(float));
+  *hq = c->take<uint8_t>(static_cast<size_t>(rows) * (I / 2));
+  *hsf = c->take<uint8_t>(sf_mma_bytes(rows, I));
+  *gs_h = c->take<float>(sizeof(float));
+  *partial = c->take<float>(kQuantMaxPartials * sizeof(float));
+  (void)H;
+  return c->off;
+}
+
+size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I) {
+  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return 0;
+  Carve c{nullptr};
+  float *h, *gs_h, *partial;
+  uint8_t *hq, *hsf;
+  int* status;
+  return forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status);
+}
+
+int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
+                      const float* gs_x, const int32_t* expert_offsets,
+                      const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
+                      float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
+                      cudaStream_t stream) {
+  if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  const int E = w->E, H = w->H, I = w->I;
+  if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (w->w1 == nullptr || w->w1_sf == nullptr || w->gs_w1 == nullptr || w->w2 == nullptr ||
+      w->w2_sf == nullptr || w->gs_w2 == nullptr || xq == nullptr || xsf_mma == nullptr ||
+      gs_x == nullptr || expert_offsets == nullptr || expert_counts == nullptr ||
+      row_token == nullptr || slot_out == nullptr || ws == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w1) || !aligned16(w->w2) || !aligned16(w->w1_sf) || !aligned16(w->w2_sf) ||
+      !aligned16(xq) || !aligned16(xsf_mma) || !aligned16(slot_out) || !aligned16(ws))
+    return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < moe_nvfp4_workspace_size(T, k, E, H, I)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (T == 0) return NVMOE_OK;
+  Carve c{static_cast<uint8_t*>(ws)};
+  float *h, *gs_h, *partial;
+  uint8_t *hq, *hsf;
+  int* status;
+  forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status);
+  float* tap_l1 = nullptr;
+  if (taps != nullptr) {
+    if (taps->h != nullptr) h = taps->h;
+    if (taps->hq != nullptr) hq = taps->hq;
+    if (taps->hsf_mma != nullptr) hsf = taps->hsf_mma;
+    if (taps->gs_h != nullptr) gs_h = taps->gs_h;
+    tap_l1 = taps->l1_out;
+    if (!aligned16(h) || !aligned16(hq) || !aligned16(hsf) || !aligned16(tap_l1))
+      return NVMOE_ERR_MISALIGNED;
+  }
+  const int64_t rows = rows_bound(T, k, E);
+  const int nsm = sm_count();
+  if (nsm <= 0) return NVMOE_ERR_CUDA;
+
+  CUtensorMap map_x, map_w1, map_h, map_w2;
+  if (!make_map(&map_x, xq, H / 2, rows) || !make_map(&map_w1, w->w1, H / 2, int64_t(E) * 2 * I) ||
+      !make_map(&map_h, hq, I / 2, rows) || !make_map(&map_w2, w->w2, I / 2, int64_t(E) * H))
+    return NVMOE_ERR_CUDA;
+
+  const int64_t max_mtiles = rows / kTileRows;
+  // L1
+  GemmArgs a1{};
+  a1.mode = 1;
+  a1.E = E;
+  a1.K = H;
+  a1.N = 2 * I;
+  a1.I = I;
+  a1.n_tiles = I / 128;
+  a1.expert_offsets = expert_offsets;
+  a1.expert_counts = expert_counts;
+  a1.a_sf = xsf_mma;
+  a1.b_sf = w->w1_sf;
+  a1.gs_a = gs_x;
+  a1.gs_b = w->gs_w1;
+  a1.out = h;
+  a1.tap = tap_l1;
+  a1.amax_partial = partial;
+  a1.status = status;
+  int64_t g1 = max_mtiles * a1.n_tiles;
+  if (g1 > nsm) g1 = nsm;
+  if (g1 < 1) g1 = 1;
+  if (g1 > kQuantMaxPartials) g1 = kQuantMaxPartials;
+  cudaError_t e = launch_gemm(a1, map_x, map_w1, static_cast<int>(g1), stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  // requantise h over the valid rows (global amax from the L1 partials)
+  e = launch_quant_pack(h, NVMOE_F32, rows, I, nullptr, 1, row_token, partial,
+                        static_cast<int>(g1), hq, nullptr, hsf, gs_h, stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  // L2
+  GemmArgs a2{};
+  a2.mode = 2;
+  a2.E = E;
+  a2.K = I;
+  a2.N = H;
+  a2.I = I;
+  a2.n_tiles = H / 256;
+  a2.expert_offsets = expert_offsets;
+  a2.expert_counts = expert_counts;
+  a2.a_sf = hsf;
+  a2.b_sf = w->w2_sf;
+  a2.gs_a = gs_h;
+  a2.gs_b = w->gs_w2;
+  a2.out = slot_out;
+  a2.tap = nullptr;
+  a2.amax_partial = nullptr;
+  a2.status = status;
+  int64_t g2 = max_mtiles * a2.n_tiles;
+  if (g2 > nsm) g2 = nsm;
+  if (g2 < 1) g2 = 1;
+  e = launch_gemm(a2, map_h, map_w2, static_cast<int>(g2), stream);
+  return status_of(e);
+}
+
+// ------------------------------------------------------------ reduce ----
+int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of, const float* topk_w,
+                         int64_t T, int k, int64_t H, void* y, int y_dtype,
+                         cudaStream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || H < 1) return NVMOE_ERR_INVALID_ARG;
+  if (y_dtype != NVMOE_BF16 && y_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return NVMOE_OK;
+  if (slot_out == nullptr || slot_of == nullptr || topk_w == nullptr || y == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(slot_out) || !aligned16(y)) return NVMOE_ERR_MISALIGNED;
+  return status_of(launch_reduce(slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Internal launchers shared between the kernel translation units and the
+// C-ABI layer (api.cu).  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace nvmoe {
+
+constexpr int kTileRows = 128;        // rows per tensor-core tile / SF atom row block
+constexpr int kSfAtomBytes = 512;     // 128 rows x 4 scale bytes
+constexpr int kStageK = 256;          // K elements per pipeline stage
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+constexpr int kQuantMaxPartials = 1024;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Byte size of a staged scale buffer for rows x cols.
+inline size_t sf_mma_bytes(int64_t rows, int64_t cols) {
+  return static_cast<size_t>(round_up(rows, kTileRows) * (round_up(cols, kStageK) / 16));
+}
+
+// ---- route ----
+cudaError_t launch_route(const int32_t* topk_ids, int64_t T, int k, int E,
+                         int32_t* expert_offsets, int32_t* expert_counts,
+                         int32_t* row_token, int64_t rows_bound, int32_t* slot_of,
+                         int32_t* chunk_counts, int n_chunks, int* status,
+                         cudaStream_t stream);
+int route_chunk_elems();
+
+// ---- quantiser ----
+// Pass 1: per-block maxima of |x| into partial[0..n_partial).
+cudaError_t launch_quant_amax(const void* x, int x_dtype, int64_t n_elems, float* partial,
+                              int n_partial, cudaStream_t stream);
+// Pass 2: reduce partial maxima -> gs; quantise rows.  row_valid (nullable)
+// skips rows whose entry is < 0.
+cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                              const int32_t* row_dst, int fanout, const int32_t* row_valid,
+                              const float* partial, int n_partial, uint8_t* q,
+                              uint8_t* sf_row, uint8_t* sf_mma, float* gs_out,
+                              cudaStream_t stream);
+int quant_amax_blocks(int64_t n_elems);
+
+// ---- weights ----
+cudaError_t launch_weight_amax(const float* w, int E, int64_t per_expert, float* partial,
+                               int parts_per_expert, cudaStream_t stream);
+cudaError_t launch_weight_quant(const float* w, int E, int K, int N, const float* partial,
+                                int parts_per_expert, uint8_t* q, uint8_t* sf, float* gs,
+                                cudaStream_t stream);
+cudaError_t launch_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int E, int K,
+                                   int N, uint8_t* q_out, uint8_t* sf_out, cudaStream_t stream);
+
+// ---- grouped GEMM ----
+struct GemmArgs {
+  int mode;               // 1: L1 (gate/up pairs, SiLU epilogue), 2: L2
+  int E;
+  int K;                  // reduction length (elements)
+  int N;                  // rows of each expert's B matrix (L1: 2I, L2: H)
+  int I;                  // L1 only: intermediate size
+  int n_tiles;            // tiles along N per expert
+  const int32_t* expert_offsets;
+  const int32_t* expert_counts;
+  const uint8_t* a_sf;    // staged, rows_bound x K
+  const uint8_t* b_sf;    // staged, E*N x K
+  const float* gs_a;      // [1]
+  const float* gs_b;      // [E]
+  float* out;             // L1: h [rows, I]; L2: slot_out [rows, N]
+  float* tap;             // L1: l1_out [rows, 2I] or null
+  float* amax_partial;    // L1: [grid]
+  int* status;
+};
+cudaError_t launch_gemm(const GemmArgs& args, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        int grid, cudaStream_t stream);
+int gemm_smem_bytes();
+
+// ---- reduce ----
+cudaError_t launch_reduce(const float* slot_out, const int32_t* slot_of, const float* topk_w,
+                          int64_t T, int k, int64_t H, void* y, int y_dtype,
+                          cudaStream_t stream);
+
+}  // namespace nvmoe

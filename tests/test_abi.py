@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point
+declared in include/*.h, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_route_gb300 import binding
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z][a-z0-9_]*)\s*\(",
+                             src, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_pipeline_calls():
+    names = declared_functions()
+    for fn in ("moe_route_permute", "nvfp4_quantize_act", "moe_nvfp4_forward",
+               "moe_unpermute_reduce"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for fn in names:
+        assert hasattr(lib, fn), fn
+
+
+def test_binding_signatures_cover_header(lib):
+    from nvfp4_block_scaled_route_gb300 import binding
+    assert set(declared_functions()) == set(binding.SIGNATURES)
+
+
+def test_host_side_helpers(lib):
+    assert lib.nvmoe_version() >= 100
+    assert lib.nvmoe_status_str(0) == b"ok"
+    assert lib.nvmoe_status_str(4) == b"workspace too small"
+    # rows bound: S + min(E, S) * 127 rounded up to 128
+    assert lib.moe_route_rows_bound(1, 8, 48) == 1024
+    assert lib.moe_route_rows_bound(0, 8, 48) == 0
+    assert lib.moe_route_rows_bound(16384, 8, 48) == 131072 + 48 * 128
+    # staged scale bytes: rows and K padded to 128 and 256
+    assert lib.nvfp4_sf_mma_bytes(1, 64) == 128 * 16
+    assert lib.nvfp4_sf_mma_bytes(129, 7168) == 256 * 448
+    assert lib.moe_nvfp4_workspace_size(1, 8, 48, 7168, 3072) > 1024 * 3072 * 4
+
+
+def test_bad_arguments_are_rejected_on_the_host(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails its checks first
+    # k out of range
+    assert lib.moe_route_permute(fake, 4, 0, 8, fake, fake, fake, fake, fake, 1 << 20, None) == 1
+    # E out of range
+    assert lib.moe_route_permute(fake, 4, 2, 300, fake, fake, fake, fake, fake, 1 << 20, None) == 1
+    # workspace too small
+    assert lib.moe_route_permute(fake, 4, 2, 8, fake, fake, fake, fake, fake, 8, None) == 4
+    # cols not a multiple of 64
+    assert lib.nvfp4_quantize_act(fake, 0, 4, 48, None, 1, 4, fake, None, None, fake, fake,
+                                  1 << 20, None) == 2
+    # bad dtype
+    assert lib.nvfp4_quantize_act(fake, 7, 4, 64, None, 1, 4, fake, None, None, fake, fake,
+                                  1 << 20, None) == 1
+    # misaligned activation pointer
+    assert lib.nvfp4_quantize_act(P((1 << 20) + 4), 0, 4, 64, None, 1, 4, fake, None, None,
+                                  fake, fake, 1 << 20, None) == 3
+    # unsupported hidden size for the forward (H % 256 != 0)
+    from nvfp4_block_scaled_route_gb300 import binding
+    w = binding.Weights(4, 320, 128, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)
+    assert lib.moe_nvfp4_forward(ctypes.byref(w), fake, fake, fake, fake, fake, fake, 1, 2,
+                                 fake, None, fake, 1 << 30, None) == 2
+    # reduce: bad dtype, bad H
+    assert lib.moe_unpermute_reduce(fake, fake, fake, 2, 2, 64, fake, 5, None) == 1
+    assert lib.moe_unpermute_reduce(fake, fake, fake, 2, 2, 60, fake, 0, None) == 2
