@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""MoE-layer tokens/s of the NVFP4 expert FFN on one GB300 (per GPU replica).
+
+One step = the whole forward pass on one batch of synthetic tokens:
+route -> quantise into the grouped slot layout -> L1 grouped GEMM with fused
+alpha/SiLU*up/amax -> requantise -> L2 grouped GEMM -> weighted reduce
+(8 kernels of libnvfp4moe.so, replayed as one CUDA graph).
+
+Default workload: the one-token decode case (E=48 experts, H=7168, I=3072,
+top-8), whose roofline is HBM bandwidth on the weight + scale bytes of the
+experts that receive a token.  The L2 cache is flushed (256 MiB write)
+before every timed step; inputs are resident in HBM before the timed region.
+
+Also reported:
+  roofline      the dominant kernel (the L1 GEMM) timed alone with CUDA events
+                recorded by the library on the launching stream, against the
+                measured HBM copy bandwidth (MEASURED_PEAKS.json)
+  e2e           the same metric through the public API from pinned host
+                buffers: H2D of x / topk ids / topk weights, forward, D2H of y
+  cpu_baseline  the CPU oracle (numpy, fp64) timed on a bounded sample of the
+                same workload (rank 0, N = 1)
+--impl reference times the oracle alone on the same workload and metric.
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+path has no cross-GPU exchange: replicas only), value = all ranks' tokens /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/sec on 1 GB300; % HBM roofline (decode), % FP4 TC peak (prefill)"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20            # > 129 MB L2
+KERNELS_PER_STEP = 8               # route 2 + quantise 2 + L1 + requant + L2 + reduce
+FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / BF16 tensor ratio on GB300
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="decode1")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--profile-steps", type=int, default=0,
+                   help="run this many eager steps and exit (for ncu launch lists)")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------ clocks ----
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------- oracle sample ----
+def _oracle_sample_worker(args):
+    """Time the oracle on `n_slots` slots of one token, each restricted to `c`
+    of the I intermediate columns (L1: c gate + c up columns; L2: c of the I
+    reduction rows), so the work is the fraction n_slots*c/(I*k) of one
+    token.  Runs in a spawned process with one BLAS thread."""
+    cfgname, c, n_slots, seed = args
+    import numpy as np
+    import torch
+    from oracle import moe as omoe
+    from oracle import nvfp4 as onv
+    from nvfp4_block_scaled_route_gb300 import synthetic as syn
+    cfg = syn.CONFIGS[cfgname]
+    H, I = cfg.H, cfg.I
+    g = torch.Generator().manual_seed(seed)
+    x = syn.draw_activations(cfg, T=1).float().numpy()
+    slots = []
+    for s in range(n_slots):
+        std = cfg.w_std * (0.5 + 1.5 * float(torch.rand(1, generator=g)))
+        w1 = (torch.randn((H, 2 * c), generator=g) * std).numpy()
+        w2 = (torch.randn((c, H), generator=g) * std).numpy()
+        slots.append((onv.quantize_weight(w1), onv.quantize_weight(w2)))
+    t0 = time.perf_counter()
+    xq, xsf, gsx = onv.quantize_rows(x)
+    y = np.zeros((1, H))
+    for (q1, s1, g1), (q2, s2, g2) in slots:
+        l1 = omoe.expert_l1(xq, xsf, gsx, q1, s1, g1)
+        h = omoe.swiglu(l1)
+        hq, hsf, gsh = onv.quantize_rows(h)
+        y += 0.125 * omoe.expert_l2(hq, hsf, gsh, q2, s2, g2)
+    t1 = time.perf_counter()
+    return t1 - t0, n_slots * c / (I * cfg.k)
+
+
+class OracleRunner:
+    """One spawned worker process (one BLAS thread) that runs oracle samples."""
+
+    ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+    def __enter__(self):
+        old = {k: os.environ.get(k) for k in self.ENV}
+        os.environ.update(self.ENV)
+        try:
+            self.pool = mp.get_context("spawn").Pool(1)
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        return self
+
+    def __exit__(self, *exc):
+        self.pool.close()
+        self.pool.join()
+
+    def sample(self, cfgname: str, c: int, n_slots: int, seed: int = 0):
+        return self.pool.apply(_oracle_sample_worker, ((cfgname, c, n_slots, seed),))
+
+    def sized(self, cfgname: str, budget_s: float, seed: int = 0):
+        """Slice width and slot count so that one sample takes about budget_s."""
+        from nvfp4_block_scaled_route_gb300 import synthetic as syn
+        cfg = syn.CONFIGS[cfgname]
+        c0 = 64
+        t, _ = self.sample(cfgname, c0, 1, seed)
+        per_col = max(t / c0, 1e-6)
+        c = int(budget_s / per_col) // 64 * 64
+        n_slots = 1
+        if c > cfg.I:
+            n_slots = min(cfg.k, max(1, int(c // cfg.I)))
+            c = cfg.I
+        return max(64, c), n_slots
+
+
+# ---------------------------------------------------------------- main ----
+def workload_desc(cfg):
+    return (f"{cfg.name}: E={cfg.E} H={cfg.H} I={cfg.I} T={cfg.T} top-{cfg.k} "
+            f"routing={cfg.routing} act={cfg.act}")
+
+
+def run_reference(args, rank, world):
+    from nvfp4_block_scaled_route_gb300 import synthetic as syn
+    cfg = syn.CONFIGS[args.config]
+    if rank != 0:
+        return
+    total_steps = args.steps + args.warmup
+    budget = max(0.05, min(20.0, 120.0 / max(total_steps, 1)))
+    times, units = [], []
+    with OracleRunner() as runner:
+        c, n_slots = runner.sized(args.config, budget)
+        for i in range(total_steps):
+            t, u = runner.sample(args.config, c, n_slots, seed=i)
+            if i >= args.warmup:
+                times.append(t)
+                units.append(u)
+    tok = sum(units)
+    sec = sum(times)
+    value = tok / sec
+    ms = 1000.0 * sec / max(len(times), 1)
+    sample = (f"per step: {n_slots} slot(s) of one token, {c} of I={cfg.I} intermediate "
+              f"columns (fraction {units[0]:.5f} of a token); value = tokens-equivalent / "
+              f"oracle seconds")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(cfg)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_route_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str):
+    """dram bytes per L1 launch from the committed ncu summary, if it was
+    taken on the current GEMM source; else None."""
+    path = os.path.join(ROOT, "profiles", "l1_gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != gemm_source_hash():
+        return None
+    return d.get("per_launch_bytes", {}).get(config)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_route_gb300 import binding as nb
+    from nvfp4_block_scaled_route_gb300 import synthetic as syn
+
+    cfg = syn.CONFIGS[args.config]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    # ---- inputs (resident in HBM) ----
+    q1s, s1s, g1s, q2s, s2s, g2s = [], [], [], [], [], []
+    for e in range(cfg.E):
+        w1 = syn.draw_weight(cfg, 1, e, device=dev)[None]
+        w2 = syn.draw_weight(cfg, 2, e, device=dev)[None]
+        q, s, g = nb.quantize_weights(w1)
+        q1s.append(q); s1s.append(s); g1s.append(g)
+        q, s, g = nb.quantize_weights(w2)
+        q2s.append(q); s2s.append(s); g2s.append(g)
+        del w1, w2
+    pw = nb.PreparedWeights.from_checkpoint(torch.cat(q1s), torch.cat(s1s), torch.cat(g1s),
+                                            torch.cat(q2s), torch.cat(s2s), torch.cat(g2s))
+    del q1s, s1s, q2s, s2s
+    x_h = syn.draw_activations(cfg).pin_memory()
+    ids_h, w_h = syn.draw_routing(cfg)
+    ids_h, w_h = ids_h.pin_memory(), w_h.pin_memory()
+    x, ids, w = x_h.to(dev), ids_h.to(dev), w_h.to(dev)
+    layer = nb.MoELayer(pw, cfg.T, cfg.k, device=dev, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+
+    active = sorted(set(ids_h.flatten().tolist()))
+    E_act = len(active)
+    H, I = cfg.H, cfg.I
+    l1_bytes = E_act * (2 * I * H // 2 + 2 * I * H // 16)
+    l2_bytes = E_act * (H * I // 2 + H * I // 16)
+    S = cfg.T * cfg.k
+    flops = 2.0 * S * H * 2 * I + 2.0 * S * I * H
+    hbm_gbs, bf16_tf, peak_src = peaks()
+
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    if args.profile_steps:
+        with torch.cuda.stream(stream):
+            for _ in range(args.profile_steps):
+                flush.fill_(1)
+                layer.forward(x, ids, w)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": args.profile_steps, "workload": workload_desc(cfg)}))
+        return
+
+    # ---- CUDA graph of one step ----
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            layer.forward(x, ids, w)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        layer.forward(x, ids, w)
+    stream.synchronize()
+    assert layer.status() == 0
+
+    def timed_loop(n, step_fn):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                starts[i].record(stream)
+                step_fn()
+                ends[i].record(stream)
+        stream.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    timed_loop(args.warmup, graph.replay)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    times = timed_loop(args.steps, graph.replay)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * cfg.T * args.steps / (total_ms / 1000.0)
+
+    # ---- dominant kernel: L1 GEMM timed alone by library-recorded events ----
+    n_prof = min(args.steps, 50)
+    stage = {"l1": [], "requant": [], "l2": []}
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            flush.fill_(i & 0xFF)
+            layer.forward(x, ids, w, taps={"stage_events": evs})
+            stream.synchronize()
+            stage["l1"].append(evs[0].elapsed_time(evs[1]))
+            stage["requant"].append(evs[1].elapsed_time(evs[2]))
+            stage["l2"].append(evs[2].elapsed_time(evs[3]))
+    l1_ms = statistics.mean(stage["l1"])
+    decode = cfg.T * cfg.k <= 2048
+    if decode:
+        achieved = l1_bytes / (l1_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "peak_source": peak_src,
+                "kernel": "grouped_gemm_kernel (L1, mode 1)",
+                "algorithmic_bytes_per_launch": l1_bytes, "launch_ms": l1_ms}
+    else:
+        l1_flops = 2.0 * S * H * 2 * I
+        achieved = l1_flops / (l1_ms / 1000.0) / 1e12
+        peak = bf16_tf * FP4_OVER_BF16
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} bf16 x {FP4_OVER_BF16} nominal fp4/bf16",
+                "kernel": "grouped_gemm_kernel (L1, mode 1)",
+                "algorithmic_flops_per_launch": l1_flops, "launch_ms": l1_ms}
+    roof["traffic"] = profiled_traffic(args.config)
+    step_bytes = l1_bytes + l2_bytes
+
+    # ---- end to end from pinned host buffers through the public API ----
+    e2e = None
+    if not args.no_e2e:
+        y_h = torch.empty((cfg.T, H), dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            x.copy_(x_h, non_blocking=True)
+            ids.copy_(ids_h, non_blocking=True)
+            w.copy_(w_h, non_blocking=True)
+            graph.replay()
+            y_h.copy_(layer.y, non_blocking=True)
+
+        timed_loop(min(args.warmup, 5), e2e_step)
+        et = timed_loop(args.steps, e2e_step)
+        e_ms = sum(et)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * cfg.T * args.steps / (e_ms / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": x_h.nbytes + ids_h.nbytes + w_h.nbytes,
+               "d2h_bytes_per_step": y_h.nbytes, "ms_per_step": e_ms / args.steps}
+    assert layer.status() == 0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        with OracleRunner() as runner:
+            c, n_slots = runner.sized(args.config, 15.0)
+            t, u = runner.sample(args.config, c, n_slots, seed=1)
+        cpu = {"value": u / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_slots} slot(s) of one token, {c} of I={I} intermediate columns "
+                         f"= {u:.5f} token-equivalents in {t:.2f} s (numpy, 1 thread)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e4m3 scales), fp32 accumulate", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "l2_flush": "256 MiB write before every step",
+                       "graph": "one CUDA graph per step", "active_experts": E_act,
+                       "algorithmic_bytes_per_step": step_bytes, "flops_per_step": flops,
+                       "step_hbm_frac": (step_bytes / (ms_per_step / 1000.0) / 1e9) / hbm_gbs,
+                       "stage_ms": {k: statistics.mean(v) for k, v in stage.items()},
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

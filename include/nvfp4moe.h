@@ -199,6 +199,9 @@ typedef struct {
  *   h        float [rows, I]:  SiLU(gate) * up (fp32)
  *   hq       uint8 [rows, I/2]; hsf_mma staged nvfp4_sf_mma_bytes(rows, I)
  *   gs_h     float [1]
+ *   stage_events  caller-created CUDA events recorded on `stream`: [0]
+ *            before the L1 GEMM, [1] after it, [2] after the requantisation,
+ *            [3] after the L2 GEMM (all four or none).
  * rows = moe_route_rows_bound(T, k, E); padding rows are unspecified.
  * When h / hq / hsf_mma / gs_h are given they replace the workspace buffers
  * of the same name (no extra traffic); l1_out costs one extra store. */
@@ -208,6 +211,7 @@ typedef struct {
   uint8_t* hq;
   uint8_t* hsf_mma;
   float* gs_h;
+  cudaEvent_t stage_events[4];
 } nvmoe_taps;
 
 /* moe_nvfp4_forward — the expert FFN on grouped slots ("NVFP4 MegaMoE Debug

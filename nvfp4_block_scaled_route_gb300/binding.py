@@ -38,7 +38,8 @@ class Weights(ctypes.Structure):
 
 class Taps(ctypes.Structure):
     _fields_ = [("l1_out", ctypes.c_void_p), ("h", ctypes.c_void_p), ("hq", ctypes.c_void_p),
-                ("hsf_mma", ctypes.c_void_p), ("gs_h", ctypes.c_void_p)]
+                ("hsf_mma", ctypes.c_void_p), ("gs_h", ctypes.c_void_p),
+                ("stage_events", ctypes.c_void_p * 4)]
 
 
 # name -> (restype, argtypes)
@@ -245,6 +246,14 @@ def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Ten
     if taps:
         t = Taps(_ptr(taps.get("l1_out")), _ptr(taps.get("h")), _ptr(taps.get("hq")),
                  _ptr(taps.get("hsf_mma")), _ptr(taps.get("gs_h")))
+        evs = taps.get("stage_events")
+        if evs is not None:
+            # torch events are created on first record; their handles are
+            # plain CUDA event handles
+            for i, ev in enumerate(evs):
+                if ev.cuda_event == 0:
+                    ev.record()
+                t.stage_events[i] = ev.cuda_event
     wst = weights.struct()
     _check("moe_nvfp4_forward", lib().moe_nvfp4_forward(
         ctypes.byref(wst), _ptr(xq), _ptr(xsf_mma), _ptr(gs_x), _ptr(route.expert_offsets),

@@ -267,7 +267,9 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   int* status;
   forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status);
   float* tap_l1 = nullptr;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   if (taps != nullptr) {
+    for (int i = 0; i < 4; ++i) ev[i] = taps->stage_events[i];
     if (taps->h != nullptr) h = taps->h;
     if (taps->hq != nullptr) hq = taps->hq;
     if (taps->hsf_mma != nullptr) hsf = taps->hsf_mma;
@@ -285,6 +287,8 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
       !make_map(&map_h, hq, I / 2, rows) || !make_map(&map_w2, w->w2, I / 2, int64_t(E) * H))
     return NVMOE_ERR_CUDA;
 
+  const bool timed = ev[0] && ev[1] && ev[2] && ev[3];
+  if (timed && cudaEventRecord(ev[0], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   const int64_t max_mtiles = rows / kTileRows;
   // L1
   GemmArgs a1{};
@@ -310,10 +314,12 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   if (g1 > kQuantMaxPartials) g1 = kQuantMaxPartials;
   cudaError_t e = launch_gemm(a1, map_x, map_w1, static_cast<int>(g1), stream);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && cudaEventRecord(ev[1], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   // requantise h over the valid rows (global amax from the L1 partials)
   e = launch_quant_pack(h, NVMOE_F32, rows, I, nullptr, 1, row_token, partial,
                         static_cast<int>(g1), hq, nullptr, hsf, gs_h, stream);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && cudaEventRecord(ev[2], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   // L2
   GemmArgs a2{};
   a2.mode = 2;
@@ -336,7 +342,9 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   if (g2 > nsm) g2 = nsm;
   if (g2 < 1) g2 = 1;
   e = launch_gemm(a2, map_h, map_w2, static_cast<int>(g2), stream);
-  return status_of(e);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && cudaEventRecord(ev[3], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  return NVMOE_OK;
 }
 
 // ------------------------------------------------------------ reduce ----

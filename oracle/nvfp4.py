@@ -49,16 +49,19 @@ def e2m1_encode(v: np.ndarray) -> np.ndarray:
     give 0x8).  Pinned: identity on all 16 codes, listed ties, brute force.
     """
     v = np.asarray(v)
-    a = np.minimum(np.abs(v.astype(np.float64)), E2M1_MAGNITUDES[-1])
+    # fp32 inputs are compared in fp32 (every magnitude and midpoint is
+    # exact there); anything else in fp64.
+    ft = np.float32 if v.dtype == np.float32 else np.float64
+    mags = E2M1_MAGNITUDES.astype(ft)
+    a = np.minimum(np.abs(v.astype(ft, copy=False)), mags[-1])
     # the two representable magnitudes around a: lo <= a <= hi
-    hi = np.minimum(np.searchsorted(E2M1_MAGNITUDES, a, side="left"), 7)
-    lo = np.maximum(hi - 1, 0)
-    dlo = a - E2M1_MAGNITUDES[lo]
-    dhi = E2M1_MAGNITUDES[hi] - a
+    hi = np.minimum(np.searchsorted(mags, a, side="left"), 7).astype(np.uint8)
+    lo = np.maximum(hi, 1) - 1
+    dlo = a - mags[lo]
+    dhi = mags[hi] - a
     pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
-    exact = E2M1_MAGNITUDES[hi] == a
-    code = np.where(exact | pick_hi, hi, lo)
-    sign = np.signbit(v).astype(np.int64)
+    code = np.where(pick_hi | (dhi == 0), hi, lo)
+    sign = np.signbit(v).astype(np.uint8)
     return (code | (sign << 3)).astype(np.uint8)
 
 
