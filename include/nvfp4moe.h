@@ -167,21 +167,29 @@ int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q,
  * later log's "B ColumnMajor" point; scale staging replaces the SF remap of
  * the commit messages on src).  Nibble pairs stay along K.
  *   q_ckpt  uint8 [E, K/2, N],  sf_ckpt uint8 [E, K/16, N]
- *   q_out   uint8 [E, N, K/2]  (K-major rows of the B operand)
+ *   q_out   K-major B-operand tiles of the [E*N, K] matrix: with
+ *           KT = ceil(K/256), row n (= e*N + column) and K-stage kt, the
+ *           contiguous 16 KB tile ((n/128)*KT + kt) holds 128 rows of 128
+ *           bytes; byte j of row n%128 packs elements 256*kt + 2j (low
+ *           nibble) and 256*kt + 2j + 1 (high); bytes past K/2 are zero.
+ *           Size moe_nvfp4_prepared_bytes(E, K, N) = E*N*KT*128.
  *   sf_out  staged scales of the [E*N, K] matrix: nvfp4_sf_mma_bytes(E*N, K)
  * Limits: K % 64 == 0, N % 128 == 0.
  */
+size_t moe_nvfp4_prepared_bytes(int E, int K, int N);
 int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt,
                               int E, int K, int N, uint8_t* q_out,
                               uint8_t* sf_out, cudaStream_t stream);
 
 /* ------------------------------------------------------------ steps 3-6 --
  * Prepared expert weights (all device pointers):
- *   w1     uint8 [E, 2I, H/2]  L1 [gate; up] rows: gate = rows [0, I),
- *          up = rows [I, 2I) of each expert (plain concatenation, commit
- *          message on the removed 2-CTA interleave)
+ *   w1     B tiles of the [E*2I, H] matrix (moe_nvfp4_prepare_weights):
+ *          L1 [gate; up] rows: gate = rows [0, I), up = rows [I, 2I) of
+ *          each expert (plain concatenation, commit message on the removed
+ *          2-CTA interleave)
  *   w1_sf  staged, nvfp4_sf_mma_bytes(E*2I, H);  gs_w1 float [E]
- *   w2     uint8 [E, H, I/2];  w2_sf staged, nvfp4_sf_mma_bytes(E*H, I);
+ *   w2     B tiles of the [E*H, I] matrix;  w2_sf staged,
+ *          nvfp4_sf_mma_bytes(E*H, I);
  *   gs_w2  float [E]
  */
 typedef struct {
@@ -227,6 +235,14 @@ typedef struct {
  *   expert_offsets, expert_counts, row_token: from moe_route_permute
  *   slot_out  float [rows, H]  (padding rows unspecified)
  * rows = moe_route_rows_bound(T, k, E).
+ * Workspace: moe_nvfp4_workspace_size bytes, zero-filled before its first
+ * use; the call leaves it ready for the next call (split-tile counters are
+ * reset by the kernel that uses them).  One workspace per stream: calls that
+ * overlap on the device must not share one.
+ * Work split: with fewer than 4 tiles per SM (decode) the tiles x K-stages
+ * sequence is divided evenly between the SMs; a tile shared by several SMs
+ * is summed in ascending K order by the last SM to finish its piece, so the
+ * result does not depend on timing.
  * Limits: H % 256 == 0, I % 128 == 0, E <= 256.
  */
 size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I);

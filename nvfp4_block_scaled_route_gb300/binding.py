@@ -57,6 +57,7 @@ SIGNATURES = {
     "nvfp4_quantize_act": (_I, [_P, _I, _I64, _I64, _P, _I, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_quantize_weights_workspace_size": (_SZ, [_I, _I, _I]),
     "nvfp4_quantize_weights": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_nvfp4_prepared_bytes": (_SZ, [_I, _I, _I]),
     "moe_nvfp4_prepare_weights": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_nvfp4_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_nvfp4_forward": (_I, [ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _I64, _I, _P,
@@ -191,11 +192,11 @@ def quantize_weights(w: torch.Tensor, stream=None):
 
 
 def prepare_weights(q_ckpt: torch.Tensor, sf_ckpt: torch.Tensor, stream=None):
-    """Checkpoint (E, K/2, N) + (E, K/16, N) -> (q [E, N, K/2], staged sf)."""
+    """Checkpoint (E, K/2, N) + (E, K/16, N) -> (B tiles, staged sf)."""
     E, K2, N = q_ckpt.shape
     K = 2 * K2
     dev = q_ckpt.device
-    q = torch.empty((E, N, K2), dtype=torch.uint8, device=dev)
+    q = torch.empty(int(lib().moe_nvfp4_prepared_bytes(E, K, N)), dtype=torch.uint8, device=dev)
     sf = torch.zeros(sf_mma_bytes(E * N, K), dtype=torch.uint8, device=dev)
     _check("moe_nvfp4_prepare_weights", lib().moe_nvfp4_prepare_weights(
         _ptr(q_ckpt), _ptr(sf_ckpt), E, K, N, _ptr(q), _ptr(sf), _stream(stream)))
@@ -226,6 +227,10 @@ class PreparedWeights:
         q2, s2 = prepare_weights(w2q, w2sf)
         return PreparedWeights(E, 2 * H2, N1 // 2, q1, s1, gs1.contiguous(), q2, s2,
                                gs2.contiguous())
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.w1, self.w1_sf, self.gs_w1, self.w2, self.w2_sf, self.gs_w2))
 
 
 # ------------------------------------------------------------- steps 3-6 --

@@ -52,6 +52,21 @@ bool make_map(CUtensorMap* map, const void* base, int64_t row_bytes, int64_t row
   return r == CUDA_SUCCESS;
 }
 
+// B-operand tiles: [n_tiles][128 rows][128 bytes] contiguous, as a 3-D map
+// with a 128 x 128 x 1 box (one 16 KB tile per load).
+bool make_tiled_map(CUtensorMap* map, const void* base, int64_t n_tiles) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>(n_tiles)};
+  cuuint64_t strides[2] = {128, 128 * 128};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -209,6 +224,11 @@ int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q, uint
   return status_of(launch_weight_quant(w, E, K, N, partial, 64, q, sf, gs, stream));
 }
 
+size_t moe_nvfp4_prepared_bytes(int E, int K, int N) {
+  if (E < 1 || K < 1 || N < 1) return 0;
+  return static_cast<size_t>(E) * N * ceil_div(K, kStageK) * 128;
+}
+
 int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int E, int K, int N,
                               uint8_t* q_out, uint8_t* sf_out, cudaStream_t stream) {
   if (E < 1 || K < 1 || N < 1 || q_ckpt == nullptr || sf_ckpt == nullptr ||
@@ -221,9 +241,13 @@ int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int
 // ----------------------------------------------------------- forward ----
 static size_t forward_layout(int64_t T, int k, int E, int H, int I, Carve* c, float** h,
                              uint8_t** hq, uint8_t** hsf, float** gs_h, float** partial,
-                             int** status) {
+                             int** status, float** pieces = nullptr, int** counters = nullptr) {
   const int64_t rows = rows_bound(T, k, E);
   *status = c->take<int>(kStatusBytes);
+  int* cnt = c->take<int>(kMaxSplitTiles * sizeof(int));
+  float* pcs = c->take<float>(static_cast<size_t>(2) * kMaxGrid * 128 * 256 * sizeof(float));
+  if (pieces != nullptr) *pieces = pcs;
+  if (counters != nullptr) *counters = cnt;
   *h = c->take<float>(static_cast<size_t>(rows) * I * sizeof(float));
   *hq = c->take<uint8_t>(static_cast<size_t>(rows) * (I / 2));
   *hsf = c->take<uint8_t>(sf_mma_bytes(rows, I));
@@ -262,10 +286,10 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   if (ws_bytes < moe_nvfp4_workspace_size(T, k, E, H, I)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
   if (T == 0) return NVMOE_OK;
   Carve c{static_cast<uint8_t*>(ws)};
-  float *h, *gs_h, *partial;
+  float *h, *gs_h, *partial, *pieces;
   uint8_t *hq, *hsf;
-  int* status;
-  forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status);
+  int *status, *counters;
+  forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status, &pieces, &counters);
   float* tap_l1 = nullptr;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   if (taps != nullptr) {
@@ -279,12 +303,16 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
       return NVMOE_ERR_MISALIGNED;
   }
   const int64_t rows = rows_bound(T, k, E);
-  const int nsm = sm_count();
+  int nsm = sm_count();
   if (nsm <= 0) return NVMOE_ERR_CUDA;
+  if (nsm > kMaxGrid) nsm = kMaxGrid;
 
   CUtensorMap map_x, map_w1, map_h, map_w2;
-  if (!make_map(&map_x, xq, H / 2, rows) || !make_map(&map_w1, w->w1, H / 2, int64_t(E) * 2 * I) ||
-      !make_map(&map_h, hq, I / 2, rows) || !make_map(&map_w2, w->w2, I / 2, int64_t(E) * H))
+  const int64_t kt1 = ceil_div(H, kStageK), kt2 = ceil_div(I, kStageK);
+  if (!make_map(&map_x, xq, H / 2, rows) ||
+      !make_tiled_map(&map_w1, w->w1, int64_t(E) * 2 * I / kTileRows * kt1) ||
+      !make_map(&map_h, hq, I / 2, rows) ||
+      !make_tiled_map(&map_w2, w->w2, int64_t(E) * H / kTileRows * kt2))
     return NVMOE_ERR_CUDA;
 
   const bool timed = ev[0] && ev[1] && ev[2] && ev[3];
@@ -307,6 +335,8 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   a1.out = h;
   a1.tap = tap_l1;
   a1.amax_partial = partial;
+  a1.partials = pieces;
+  a1.counters = counters;
   a1.status = status;
   int64_t g1 = max_mtiles * a1.n_tiles;
   if (g1 > nsm) g1 = nsm;
@@ -337,6 +367,8 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   a2.out = slot_out;
   a2.tap = nullptr;
   a2.amax_partial = nullptr;
+  a2.partials = pieces;
+  a2.counters = counters;
   a2.status = status;
   int64_t g2 = max_mtiles * a2.n_tiles;
   if (g2 > nsm) g2 = nsm;

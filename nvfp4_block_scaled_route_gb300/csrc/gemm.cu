@@ -80,7 +80,113 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
   return ti;
 }
 
+// Work partition.  With many tiles (>= kStreamKFactor per CTA) CTAs take
+// whole tiles round-robin.  With few tiles (decode) the tiles x K-stages
+// sequence is cut into gridDim.x equal contiguous ranges ("stream-K"): a
+// tile split between CTAs is summed by the CTA that finishes it last, in
+// ascending K order (deterministic), from fp32 partials in the workspace.
+constexpr int kStreamKFactor = 4;
+
+struct WorkIter {
+  bool stream_k;
+  int total, ks, G;
+  int64_t cur, end;   // stream-K: linear stage units
+  int t;              // round-robin: next tile
+
+  __device__ void init(int total_tiles, int k_stages, int grid, int cta) {
+    total = total_tiles;
+    ks = k_stages;
+    G = grid;
+    stream_k = total_tiles < kStreamKFactor * grid;
+    const int64_t W = static_cast<int64_t>(total_tiles) * k_stages;
+    cur = end = 0;
+    t = cta;
+    if (stream_k) {
+      // never more ranges than stage units, so that every range is non-empty
+      // and the CTAs c_first..c_last of a tile all hold a piece of it
+      if (W < G) G = static_cast<int>(W);
+      if (cta < G) {
+        cur = W * cta / G;
+        end = W * (cta + 1) / G;
+      }
+    }
+  }
+  __device__ bool next(int& tile, int& s0, int& s1) {
+    if (!stream_k) {
+      if (t >= total) return false;
+      tile = t;
+      s0 = 0;
+      s1 = ks;
+      t += G;
+      return true;
+    }
+    if (cur >= end) return false;
+    tile = static_cast<int>(cur / ks);
+    s0 = static_cast<int>(cur - static_cast<int64_t>(tile) * ks);
+    const int64_t lim = end - static_cast<int64_t>(tile) * ks;
+    s1 = lim < ks ? static_cast<int>(lim) : ks;
+    cur = static_cast<int64_t>(tile) * ks + s1;
+    return true;
+  }
+  // CTA whose range holds stage unit u
+  __device__ int owner(int64_t u) const {
+    const int64_t W = static_cast<int64_t>(total) * ks;
+    return static_cast<int>(((u + 1) * G + W - 1) / W - 1);
+  }
+  __device__ int first_tile(int cta) const {
+    const int64_t W = static_cast<int64_t>(total) * ks;
+    return static_cast<int>(W * cta / G / ks);
+  }
+  // partial slot of CTA c's piece of tile t (a CTA holds at most two pieces)
+  __device__ int slot(int c, int tile) const { return 2 * c + (tile == first_tile(c) ? 0 : 1); }
+};
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// L1 epilogue on 32 columns: gate g[] and up u[] (raw accumulators).
+__device__ __forceinline__ void epi_l1(const float (&g)[32], const float (&u)[32], float alpha,
+                                       int64_t row, int col, const GemmArgs& args, float& amax) {
+  const int I = args.I;
+  float* hp = args.out + row * I + col;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    float gv[4], uv[4], hv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gv[j] = __fmul_rn(alpha, g[i + j]);
+      uv[j] = __fmul_rn(alpha, u[i + j]);
+      hv[j] = __fmul_rn(silu_f(gv[j]), uv[j]);
+      amax = fmaxf(amax, fabsf(hv[j]));
+    }
+    *reinterpret_cast<float4*>(hp + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    if (args.tap != nullptr) {
+      float* tp = args.tap + row * (2 * I) + col + i;
+      *reinterpret_cast<float4*>(tp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+      *reinterpret_cast<float4*>(tp + I) = make_float4(uv[0], uv[1], uv[2], uv[3]);
+    }
+  }
+}
+
+// L2 epilogue on 32 columns.
+__device__ __forceinline__ void epi_l2(const float (&a)[32], float alpha, int64_t row, int col,
+                                       const GemmArgs& args) {
+  float* op = args.out + row * args.N + col;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4)
+    *reinterpret_cast<float4*>(op + i) =
+        make_float4(__fmul_rn(alpha, a[i]), __fmul_rn(alpha, a[i + 1]),
+                    __fmul_rn(alpha, a[i + 2]), __fmul_rn(alpha, a[i + 3]));
+}
+
+__device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -96,6 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   __shared__ int s_off[kMaxExperts];
   __shared__ int s_cnt[kMaxExperts];
   __shared__ float s_amax[4];
+  __shared__ int s_last;
+  __shared__ int s_ok;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
@@ -141,6 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   const int k_blocks = args.K / 64;
   const int k_stages = (args.K + kStageK - 1) / kStageK;
   const int k_atoms = k_stages * 4;
+  WorkIter it;
+  it.init(total_tiles, k_stages, gridDim.x, blockIdx.x);
+  int tile, s0, s1;
 
   if (warp == 0) {
     // ------------------------------------------------------- producer --
@@ -151,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, s_prefix, s_mtiles, E);
+      while (ok && it.next(tile, s0, s1)) {
+        const TileInfo ti = decode_tile(tile, s_prefix, s_mtiles, E);
         const int a_row = s_off[ti.e] + ti.mt * kBM;
         int b_row0, b_row1;
         if (args.mode == 1) {
@@ -162,10 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           b_row0 = ti.e * args.N + ti.nt * kBN;
           b_row1 = b_row0 + 128;
         }
+        // B is stored as contiguous 16 KB tiles (128 rows x one K-stage)
+        const int b_tile0 = (b_row0 / 128) * k_stages;
+        const int b_tile1 = (b_row1 / 128) * k_stages;
         const uint8_t* sfa = args.a_sf + (static_cast<size_t>(a_row / 128) * k_atoms) * kSfAtomBytes;
         const uint8_t* sfb0 = args.b_sf + (static_cast<size_t>(b_row0 / 128) * k_atoms) * kSfAtomBytes;
         const uint8_t* sfb1 = args.b_sf + (static_cast<size_t>(b_row1 / 128) * k_atoms) * kSfAtomBytes;
-        for (int ks = 0; ks < k_stages; ++ks) {
+        for (int ks = s0; ks < s1; ++ks) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, args.status, abort)) {
             ok = false;
             break;
@@ -174,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           mbar_arrive_expect_tx(full, kStageTx);
           const int32_t x = ks * kRowBytes;
           tma_load_2d(smem + kOffA + stage * kABytes, &map_a, x, a_row, full, pol_a);
-          tma_load_2d(smem + kOffB + stage * kBBytes, &map_b, x, b_row0, full, pol_b);
-          tma_load_2d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, x, b_row1, full,
-                      pol_b);
+          tma_load_3d(smem + kOffB + stage * kBBytes, &map_b, 0, 0, b_tile0 + ks, full, pol_b);
+          tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, 0, 0, b_tile1 + ks,
+                      full, pol_b);
           const size_t koff = static_cast<size_t>(ks) * 4 * kSfAtomBytes;
           bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + koff, kSfaBytes, full, pol_a);
           bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb0 + koff, kSfaBytes, full, pol_b);
@@ -207,10 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      while (ok && it.next(tile, s0, s1)) {
         if (!mbar_wait(&bars->acc_empty, acc_phase ^ 1u, args.status, abort)) break;
         tc_fence_after();
-        for (int ks = 0; ks < k_stages; ++ks) {
+        for (int ks = s0; ks < s1; ++ks) {
           if (!mbar_wait(&bars->full[stage], phase, args.status, abort)) {
             ok = false;
             break;
@@ -233,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             const uint64_t adesc = smem_desc(a_base + kb * 32, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(b_base + kb * 32, 16, 1024, 2);
             mma_mxf4nvf4(tmem, adesc, bdesc, idesc, sfa_t + kb * 4, sfb_t + kb * 8,
-                         (ks | kb) != 0 ? 1u : 0u);
+                         (ks != s0 || kb != 0) ? 1u : 0u);
           }
           tc_commit(&bars->empty[stage]);
           if (++stage == kStages) {
@@ -255,80 +369,104 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const int q = warp & 3;                      // TMEM lane quarter
     const int row_in_tile = q * 32 + lane;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const bool lead = warp == 2 && lane == 0;
     float amax = 0.0f;
     uint32_t acc_phase = 0;
     const float gs_a = *args.gs_a;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(t, s_prefix, s_mtiles, E);
+    while (it.next(tile, s0, s1)) {
+      const TileInfo ti = decode_tile(tile, s_prefix, s_mtiles, E);
       const float alpha = __fmul_rn(gs_a, args.gs_b[ti.e]);
-      if (!mbar_wait(&bars->acc_full, acc_phase, args.status, abort)) break;
+      // one thread waits (bounded) and the decision is shared, so the four
+      // epilogue warps always take the same path through the named barriers
+      if (lead) s_ok = mbar_wait(&bars->acc_full, acc_phase, args.status, abort) ? 1 : 0;
+      epi_bar();
+      if (!s_ok) break;
       tc_fence_after();
       const bool valid = ti.mt * kBM + row_in_tile < s_cnt[ti.e];
       const int64_t row = s_off[ti.e] + ti.mt * kBM + row_in_tile;
-      if (args.mode == 1) {
-        const int I = args.I;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, g);
-          tmem_ld_32x32b_x32(t_row + 128 + c * 32, u);
-          tmem_ld_wait();
-          if (valid) {
-            const int col = ti.nt * 128 + c * 32;
-            float* hp = args.out + row * I + col;
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              float4 hv;
-              float gv[4], uv[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                gv[j] = __fmul_rn(alpha, __uint_as_float(g[i + j]));
-                uv[j] = __fmul_rn(alpha, __uint_as_float(u[i + j]));
-              }
-              hv.x = __fmul_rn(silu_f(gv[0]), uv[0]);
-              hv.y = __fmul_rn(silu_f(gv[1]), uv[1]);
-              hv.z = __fmul_rn(silu_f(gv[2]), uv[2]);
-              hv.w = __fmul_rn(silu_f(gv[3]), uv[3]);
-              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)),
-                                       fmaxf(fabsf(hv.z), fabsf(hv.w))));
-              *reinterpret_cast<float4*>(hp + i) = hv;
-              if (args.tap != nullptr) {
-                float* tp = args.tap + row * (2 * I) + col + i;
-                *reinterpret_cast<float4*>(tp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
-                *reinterpret_cast<float4*>(tp + I) = make_float4(uv[0], uv[1], uv[2], uv[3]);
-              }
-            }
+      const int col0 = ti.nt * (args.mode == 1 ? 128 : kBN);
+      if (s0 == 0 && s1 == k_stages) {
+        // whole tile in this CTA: epilogue straight from TMEM
+        if (args.mode == 1) {
+          for (int c = 0; c < 4; ++c) {
+            float g[32], u[32];
+            tmem_ld_f32(t_row + c * 32, g);
+            tmem_ld_f32(t_row + 128 + c * 32, u);
+            if (valid) epi_l1(g, u, alpha, row, col0 + c * 32, args, amax);
+          }
+        } else {
+          for (int c = 0; c < 8; ++c) {
+            float a[32];
+            tmem_ld_f32(t_row + c * 32, a);
+            if (valid) epi_l2(a, alpha, row, col0 + c * 32, args);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->acc_empty);
       } else {
-        const int N = args.N;
+        // a piece of a split tile: park the raw accumulator in the workspace
+        float* mine = args.partials +
+                      (static_cast<size_t>(it.slot(blockIdx.x, tile)) * kBM + row_in_tile) * kBN;
         for (int c = 0; c < 8; ++c) {
-          uint32_t a[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, a);
-          tmem_ld_wait();
+          float a[32];
+          tmem_ld_f32(t_row + c * 32, a);
           if (valid) {
-            float* op = args.out + row * N + ti.nt * kBN + c * 32;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              *reinterpret_cast<float4*>(op + i) =
-                  make_float4(__fmul_rn(alpha, __uint_as_float(a[i])),
-                              __fmul_rn(alpha, __uint_as_float(a[i + 1])),
-                              __fmul_rn(alpha, __uint_as_float(a[i + 2])),
-                              __fmul_rn(alpha, __uint_as_float(a[i + 3])));
+            for (int i = 0; i < 32; i += 4)
+              __stcg(reinterpret_cast<float4*>(mine + c * 32 + i),
+                     make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->acc_empty);
+        __threadfence();
+        epi_bar();
+        const int64_t u_first = static_cast<int64_t>(tile) * k_stages;
+        const int c_first = it.owner(u_first);
+        const int c_last = it.owner(u_first + k_stages - 1);
+        if (lead) s_last = atomicAdd(&args.counters[tile], 1) == c_last - c_first;
+        epi_bar();
+        if (s_last) {
+          // every piece has landed: sum them in ascending K order
+          __threadfence();
+          if (lead) args.counters[tile] = 0;
+          if (valid) {
+            const int nch = args.mode == 1 ? 4 : 8;
+            for (int c = 0; c < nch; ++c) {
+              float a[32], b[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.0f;
+              for (int cc = c_first; cc <= c_last; ++cc) {
+                const float* p = args.partials +
+                                 (static_cast<size_t>(it.slot(cc, tile)) * kBM + row_in_tile) * kBN;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(p + c * 32 + i));
+                  a[i] += v.x; a[i + 1] += v.y; a[i + 2] += v.z; a[i + 3] += v.w;
+                  if (args.mode == 1) {
+                    const float4 w = __ldcg(reinterpret_cast<const float4*>(p + 128 + c * 32 + i));
+                    b[i] += w.x; b[i + 1] += w.y; b[i + 2] += w.z; b[i + 3] += w.w;
+                  }
+                }
+              }
+              if (args.mode == 1)
+                epi_l1(a, b, alpha, row, col0 + c * 32, args, amax);
+              else
+                epi_l2(a, alpha, row, col0 + c * 32, args);
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty);
       acc_phase ^= 1u;
     }
     if (args.mode == 1) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
       if (lane == 0) s_amax[q] = amax;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (warp == 2 && lane == 0)
+      epi_bar();
+      if (lead)
         args.amax_partial[blockIdx.x] =
             fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
     }

@@ -71,8 +71,12 @@ struct GemmArgs {
   float* out;             // L1: h [rows, I]; L2: slot_out [rows, N]
   float* tap;             // L1: l1_out [rows, 2I] or null
   float* amax_partial;    // L1: [grid]
+  float* partials;        // split-tile pieces: [2 * grid][128][256] fp32
+  int* counters;          // split-tile arrival counts: [kMaxSplitTiles], zero between calls
   int* status;
 };
+constexpr int kMaxGrid = 256;
+constexpr int kMaxSplitTiles = 4 * kMaxGrid;
 cudaError_t launch_gemm(const GemmArgs& args, const CUtensorMap& map_a, const CUtensorMap& map_b,
                         int grid, cudaStream_t stream);
 int gemm_smem_bytes();

@@ -243,23 +243,29 @@ __global__ void __launch_bounds__(kPackThreads) weight_quant_kernel(
   sf[(static_cast<int64_t>(e) * (K / 16) + kb) * N + n] = static_cast<uint8_t>(s);
 }
 
-// Checkpoint (K/2, N) bytes -> K-major (N, K/2) bytes, 32x32 byte tiles.
-__global__ void transpose_bytes_kernel(const uint8_t* __restrict__ src, int R, int C,
-                                       uint8_t* __restrict__ dst) {
-  // src: [E][R][C] -> dst: [E][C][R]
+// Checkpoint (K/2, N) bytes of expert e -> B-operand tiles: row n of the
+// (E*N, K) matrix, K-stage kt (128 bytes) lives in the contiguous 16 KB tile
+// ((n_global / 128) * KT + kt), at row n % 128.  Bytes past K/2 are zero.
+// 32x32 byte tiles through shared memory.
+__global__ void tile_weight_bytes_kernel(const uint8_t* __restrict__ src, int R, int C, int KT,
+                                         uint8_t* __restrict__ dst) {
+  // src: [E][R = K/2][C = N];  grid.y covers the padded R (KT * 128)
   __shared__ uint8_t tile[32][33];
   const int e = blockIdx.z;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   const uint8_t* s = src + static_cast<int64_t>(e) * R * C;
-  uint8_t* d = dst + static_cast<int64_t>(e) * R * C;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int r = r0 + i, c = c0 + threadIdx.x;
-    if (r < R && c < C) tile[i][threadIdx.x] = s[static_cast<int64_t>(r) * C + c];
+    if (c < C) tile[i][threadIdx.x] = r < R ? s[static_cast<int64_t>(r) * C + c] : 0;
   }
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int c = c0 + i, r = r0 + threadIdx.x;
-    if (r < R && c < C) d[static_cast<int64_t>(c) * R + r] = tile[threadIdx.x][i];
+    if (c >= C) continue;
+    const int64_t n = static_cast<int64_t>(e) * C + c;
+    const int64_t off = ((n / kTileRows) * KT + r / 128) * (kTileRows * 128) +
+                        (n % kTileRows) * 128 + (r % 128);
+    dst[off] = tile[threadIdx.x][i];
   }
 }
 
@@ -337,9 +343,9 @@ cudaError_t launch_weight_quant(const float* w, int E, int K, int N, const float
 
 cudaError_t launch_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int E, int K,
                                    int N, uint8_t* q_out, uint8_t* sf_out, cudaStream_t stream) {
-  dim3 tgrid(static_cast<unsigned>(ceil_div(N, 32)), static_cast<unsigned>(ceil_div(K / 2, 32)),
-             E);
-  transpose_bytes_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(q_ckpt, K / 2, N, q_out);
+  const int KT = static_cast<int>(ceil_div(K, kStageK));
+  dim3 tgrid(static_cast<unsigned>(ceil_div(N, 32)), static_cast<unsigned>(KT * 4), E);
+  tile_weight_bytes_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(q_ckpt, K / 2, N, KT, q_out);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int k_atoms = static_cast<int>(round_up(K, kStageK) / 64);

@@ -179,13 +179,20 @@ def test_quantize_weights_bit_exact(nb, E, K, N):
         assert np.array_equal(sf[e].cpu().numpy(), osf)
 
 
-def test_prepare_weights_layout(nb):
+@pytest.mark.parametrize("E,K,N", [(2, 512, 256), (3, 128, 384), (1, 768, 128)])
+def test_prepare_weights_layout(nb, E, K, N):
+    """B tiles: byte j of row n in K-stage kt at ((n/128)*KT + kt)*16384 +
+    (n%128)*128 + j, zero past K/2; scales staged per the header formula."""
     rng = np.random.default_rng(4)
-    E, K, N = 2, 512, 256
     q = rng.integers(0, 256, (E, K // 2, N), dtype=np.uint8)
     sf = rng.integers(0, 127, (E, K // 16, N), dtype=np.uint8)
     qo, sfo = nb.prepare_weights(torch.from_numpy(q).to(DEV), torch.from_numpy(sf).to(DEV))
-    assert np.array_equal(qo.cpu().numpy(), q.transpose(0, 2, 1))
+    KT = -(-K // 256)
+    rows = q.transpose(0, 2, 1).reshape(E * N, K // 2)          # K-major rows
+    padded = np.zeros((E * N, KT * 128), np.uint8)
+    padded[:, :K // 2] = rows
+    want = padded.reshape(E * N // 128, 128, KT, 128).transpose(0, 2, 1, 3).reshape(-1)
+    assert np.array_equal(qo.cpu().numpy(), want)
     sf_rows = sf.transpose(0, 2, 1).reshape(E * N, K // 16)
     assert np.array_equal(unstage(sfo.cpu().numpy(), E * N, K), sf_rows)
 
