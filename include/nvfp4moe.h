@@ -209,10 +209,19 @@ typedef struct {
  *   gs_h     float [1]
  *   stage_events  caller-created CUDA events recorded on `stream`: [0]
  *            before the L1 GEMM, [1] after it, [2] after the requantisation,
- *            [3] after the L2 GEMM (all four or none).
+ *            [3] after the L2 GEMM (all four or none; on the fused path
+ *            [1..3] are all recorded after the single kernel).
+ *   path     NVMOE_PATH_AUTO (0, default), NVMOE_PATH_SEPARATE (three
+ *            launches: L1, requantisation, L2) or NVMOE_PATH_FUSED (one
+ *            cooperative kernel with two grid barriers).  AUTO takes the
+ *            fused kernel when both GEMMs have fewer than 4 tiles per SM.
+ *            Both paths compute identical results.
  * rows = moe_route_rows_bound(T, k, E); padding rows are unspecified.
  * When h / hq / hsf_mma / gs_h are given they replace the workspace buffers
  * of the same name (no extra traffic); l1_out costs one extra store. */
+#define NVMOE_PATH_AUTO 0
+#define NVMOE_PATH_SEPARATE 1
+#define NVMOE_PATH_FUSED 2
 typedef struct {
   float* l1_out;
   float* h;
@@ -220,6 +229,7 @@ typedef struct {
   uint8_t* hsf_mma;
   float* gs_h;
   cudaEvent_t stage_events[4];
+  int path;
 } nvmoe_taps;
 
 /* moe_nvfp4_forward — the expert FFN on grouped slots ("NVFP4 MegaMoE Debug

@@ -39,7 +39,10 @@ class Weights(ctypes.Structure):
 class Taps(ctypes.Structure):
     _fields_ = [("l1_out", ctypes.c_void_p), ("h", ctypes.c_void_p), ("hq", ctypes.c_void_p),
                 ("hsf_mma", ctypes.c_void_p), ("gs_h", ctypes.c_void_p),
-                ("stage_events", ctypes.c_void_p * 4)]
+                ("stage_events", ctypes.c_void_p * 4), ("path", ctypes.c_int)]
+
+
+PATH_AUTO, PATH_SEPARATE, PATH_FUSED = 0, 1, 2
 
 
 # name -> (restype, argtypes)
@@ -259,6 +262,7 @@ def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Ten
                 if ev.cuda_event == 0:
                     ev.record()
                 t.stage_events[i] = ev.cuda_event
+        t.path = int(taps.get("path", PATH_AUTO))
     wst = weights.struct()
     _check("moe_nvfp4_forward", lib().moe_nvfp4_forward(
         ctypes.byref(wst), _ptr(xq), _ptr(xsf_mma), _ptr(gs_x), _ptr(route.expert_offsets),

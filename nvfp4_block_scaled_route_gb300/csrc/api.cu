@@ -4,7 +4,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/nvfp4moe.h"
+#include "nvfp4moe.h"
 #include "internal.h"
 
 using namespace nvmoe;
@@ -239,31 +239,37 @@ int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int
 }
 
 // ----------------------------------------------------------- forward ----
-static size_t forward_layout(int64_t T, int k, int E, int H, int I, Carve* c, float** h,
-                             uint8_t** hq, uint8_t** hsf, float** gs_h, float** partial,
-                             int** status, float** pieces = nullptr, int** counters = nullptr) {
+struct FwdBuffers {
+  int* status;
+  int* counters;      // [2][kMaxSplitTiles]: split-tile arrivals of L1 and of L2
+  int* grid_bar;      // fused kernel's grid barrier words
+  float* pieces;      // split-tile partial accumulators
+  float* h;
+  uint8_t* hq;
+  uint8_t* hsf;
+  float* gs_h;
+  float* amax;        // per-CTA maxima of |h|
+};
+
+static size_t forward_layout(int64_t T, int k, int E, int I, uint8_t* base, FwdBuffers* b) {
+  Carve c{base};
   const int64_t rows = rows_bound(T, k, E);
-  *status = c->take<int>(kStatusBytes);
-  int* cnt = c->take<int>(kMaxSplitTiles * sizeof(int));
-  float* pcs = c->take<float>(static_cast<size_t>(2) * kMaxGrid * 128 * 256 * sizeof(float));
-  if (pieces != nullptr) *pieces = pcs;
-  if (counters != nullptr) *counters = cnt;
-  *h = c->take<float>(static_cast<size_t>(rows) * I * sizeof(float));
-  *hq = c->take<uint8_t>(static_cast<size_t>(rows) * (I / 2));
-  *hsf = c->take<uint8_t>(sf_mma_bytes(rows, I));
-  *gs_h = c->take<float>(sizeof(float));
-  *partial = c->take<float>(kQuantMaxPartials * sizeof(float));
-  (void)H;
-  return c->off;
+  b->status = c.take<int>(kStatusBytes);
+  b->counters = c.take<int>(2 * kMaxSplitTiles * sizeof(int));
+  b->grid_bar = c.take<int>(2 * sizeof(int));
+  b->pieces = c.take<float>(static_cast<size_t>(2) * kMaxGrid * 128 * 256 * sizeof(float));
+  b->h = c.take<float>(static_cast<size_t>(rows) * I * sizeof(float));
+  b->hq = c.take<uint8_t>(static_cast<size_t>(rows) * (I / 2));
+  b->hsf = c.take<uint8_t>(sf_mma_bytes(rows, I));
+  b->gs_h = c.take<float>(sizeof(float));
+  b->amax = c.take<float>(kQuantMaxPartials * sizeof(float));
+  return c.off;
 }
 
 size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I) {
   if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return 0;
-  Carve c{nullptr};
-  float *h, *gs_h, *partial;
-  uint8_t *hq, *hsf;
-  int* status;
-  return forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status);
+  FwdBuffers b;
+  return forward_layout(T, k, E, I, nullptr, &b);
 }
 
 int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
@@ -284,22 +290,23 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
       !aligned16(xq) || !aligned16(xsf_mma) || !aligned16(slot_out) || !aligned16(ws))
     return NVMOE_ERR_MISALIGNED;
   if (ws_bytes < moe_nvfp4_workspace_size(T, k, E, H, I)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  int path = NVMOE_PATH_AUTO;
+  if (taps != nullptr) path = taps->path;
+  if (path != NVMOE_PATH_AUTO && path != NVMOE_PATH_SEPARATE && path != NVMOE_PATH_FUSED)
+    return NVMOE_ERR_INVALID_ARG;
   if (T == 0) return NVMOE_OK;
-  Carve c{static_cast<uint8_t*>(ws)};
-  float *h, *gs_h, *partial, *pieces;
-  uint8_t *hq, *hsf;
-  int *status, *counters;
-  forward_layout(T, k, E, H, I, &c, &h, &hq, &hsf, &gs_h, &partial, &status, &pieces, &counters);
+  FwdBuffers b;
+  forward_layout(T, k, E, I, static_cast<uint8_t*>(ws), &b);
   float* tap_l1 = nullptr;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   if (taps != nullptr) {
     for (int i = 0; i < 4; ++i) ev[i] = taps->stage_events[i];
-    if (taps->h != nullptr) h = taps->h;
-    if (taps->hq != nullptr) hq = taps->hq;
-    if (taps->hsf_mma != nullptr) hsf = taps->hsf_mma;
-    if (taps->gs_h != nullptr) gs_h = taps->gs_h;
+    if (taps->h != nullptr) b.h = taps->h;
+    if (taps->hq != nullptr) b.hq = taps->hq;
+    if (taps->hsf_mma != nullptr) b.hsf = taps->hsf_mma;
+    if (taps->gs_h != nullptr) b.gs_h = taps->gs_h;
     tap_l1 = taps->l1_out;
-    if (!aligned16(h) || !aligned16(hq) || !aligned16(hsf) || !aligned16(tap_l1))
+    if (!aligned16(b.h) || !aligned16(b.hq) || !aligned16(b.hsf) || !aligned16(tap_l1))
       return NVMOE_ERR_MISALIGNED;
   }
   const int64_t rows = rows_bound(T, k, E);
@@ -311,14 +318,10 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   const int64_t kt1 = ceil_div(H, kStageK), kt2 = ceil_div(I, kStageK);
   if (!make_map(&map_x, xq, H / 2, rows) ||
       !make_tiled_map(&map_w1, w->w1, int64_t(E) * 2 * I / kTileRows * kt1) ||
-      !make_map(&map_h, hq, I / 2, rows) ||
+      !make_map(&map_h, b.hq, I / 2, rows) ||
       !make_tiled_map(&map_w2, w->w2, int64_t(E) * H / kTileRows * kt2))
     return NVMOE_ERR_CUDA;
 
-  const bool timed = ev[0] && ev[1] && ev[2] && ev[3];
-  if (timed && cudaEventRecord(ev[0], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
-  const int64_t max_mtiles = rows / kTileRows;
-  // L1
   GemmArgs a1{};
   a1.mode = 1;
   a1.E = E;
@@ -332,25 +335,12 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   a1.b_sf = w->w1_sf;
   a1.gs_a = gs_x;
   a1.gs_b = w->gs_w1;
-  a1.out = h;
+  a1.out = b.h;
   a1.tap = tap_l1;
-  a1.amax_partial = partial;
-  a1.partials = pieces;
-  a1.counters = counters;
-  a1.status = status;
-  int64_t g1 = max_mtiles * a1.n_tiles;
-  if (g1 > nsm) g1 = nsm;
-  if (g1 < 1) g1 = 1;
-  if (g1 > kQuantMaxPartials) g1 = kQuantMaxPartials;
-  cudaError_t e = launch_gemm(a1, map_x, map_w1, static_cast<int>(g1), stream);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
-  if (timed && cudaEventRecord(ev[1], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
-  // requantise h over the valid rows (global amax from the L1 partials)
-  e = launch_quant_pack(h, NVMOE_F32, rows, I, nullptr, 1, row_token, partial,
-                        static_cast<int>(g1), hq, nullptr, hsf, gs_h, stream);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
-  if (timed && cudaEventRecord(ev[2], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
-  // L2
+  a1.amax_partial = b.amax;
+  a1.partials = b.pieces;
+  a1.counters = b.counters;
+  a1.status = b.status;
   GemmArgs a2{};
   a2.mode = 2;
   a2.E = E;
@@ -360,20 +350,52 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   a2.n_tiles = H / 256;
   a2.expert_offsets = expert_offsets;
   a2.expert_counts = expert_counts;
-  a2.a_sf = hsf;
+  a2.a_sf = b.hsf;
   a2.b_sf = w->w2_sf;
-  a2.gs_a = gs_h;
+  a2.gs_a = b.gs_h;
   a2.gs_b = w->gs_w2;
   a2.out = slot_out;
   a2.tap = nullptr;
   a2.amax_partial = nullptr;
-  a2.partials = pieces;
-  a2.counters = counters;
-  a2.status = status;
-  int64_t g2 = max_mtiles * a2.n_tiles;
-  if (g2 > nsm) g2 = nsm;
-  if (g2 < 1) g2 = 1;
-  e = launch_gemm(a2, map_h, map_w2, static_cast<int>(g2), stream);
+  a2.partials = b.pieces;
+  a2.counters = b.counters + kMaxSplitTiles;
+  a2.status = b.status;
+
+  // Tiles that can exist, from the host-side bound on expert segments.
+  const int64_t S = T * k;
+  const int64_t mt_bound = S / kTileRows + (S < E ? S : E);
+  const int64_t tiles1 = mt_bound * a1.n_tiles, tiles2 = mt_bound * a2.n_tiles;
+  auto grid_for = [&](int64_t tiles) {
+    int64_t g = tiles < nsm ? tiles : nsm;
+    return static_cast<int>(g < 1 ? 1 : g);
+  };
+  // Few tiles (decode): one cooperative kernel for L1 -> requantise -> L2.
+  const bool fused = path == NVMOE_PATH_FUSED ||
+                     (path == NVMOE_PATH_AUTO && tiles1 < 4 * int64_t(nsm) && tiles2 < 4 * int64_t(nsm));
+  const bool timed = ev[0] && ev[1] && ev[2] && ev[3];
+  if (timed && cudaEventRecord(ev[0], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (fused) {
+    const int g = grid_for(tiles1 > tiles2 ? tiles1 : tiles2);
+    cudaError_t e = launch_fused_ffn(a1, a2, map_x, map_w1, map_h, map_w2, b.grid_bar, row_token,
+                                     b.hq, b.hsf, b.gs_h, g, stream);
+    if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+    if (timed) {
+      // one kernel: L1, requantisation and L2 are not separable
+      for (int i = 1; i < 4; ++i)
+        if (cudaEventRecord(ev[i], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+    }
+    return NVMOE_OK;
+  }
+  const int g1 = grid_for(tiles1);
+  cudaError_t e = launch_gemm(a1, map_x, map_w1, g1, stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && cudaEventRecord(ev[1], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  // requantise h over the valid rows (global amax from the L1 partials)
+  e = launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1, b.hq, nullptr,
+                        b.hsf, b.gs_h, stream);
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && cudaEventRecord(ev[2], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  e = launch_gemm(a2, map_h, map_w2, grid_for(tiles2), stream);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
   if (timed && cudaEventRecord(ev[3], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   return NVMOE_OK;

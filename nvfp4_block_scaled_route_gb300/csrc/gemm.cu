@@ -11,11 +11,20 @@
 // ("NVFP4 MegaMoE Debug Log", NVFP4 MoE Pipeline: the L1/L2 GEMMs with
 // per-expert alpha, SiLU(gate)*up on the plain [gate; up] halves.)
 //
+// Two kernels share the role code below:
+//   grouped_gemm_kernel   one GEMM (L1 or L2) per launch
+//   fused_ffn_kernel      cooperative launch for the few-tile (decode) case:
+//                         L1 -> grid barrier -> requantise h -> grid barrier
+//                         -> L2 in one persistent kernel; the producer starts
+//                         loading L2 weights while the L1 tail and the
+//                         requantisation are still running.
+//
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer (A tile, two 128-row B tiles, staged scales)
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM)
 //               and tcgen05.mma
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, one row per thread
+//               (and the requantisation in the fused kernel)
 //
 // Shared memory per stage (K = 256 elements = 128 bytes per row):
 //   A 128 rows x 128 B (16 KB), B 256 rows x 128 B (32 KB), both in the
@@ -25,6 +34,7 @@
 // stage s at 256 + 48 s: SFA 4 columns per 64-element k-block, SFB 8.
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace nvmoe {
 
@@ -50,6 +60,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kTmemSfStage = 48;
+constexpr int kGatePrefetchStages = 16;   // fused kernel: L2 weights prefetched while gated
 
 struct __align__(8) Barriers {
   uint64_t full[kStages];
@@ -64,6 +75,16 @@ static_assert(sizeof(Barriers) <= 256, "barrier block");
 
 struct TileInfo {
   int e, nt, mt;
+};
+
+// Per-expert tables shared by every role (in shared memory).
+struct Tables {
+  int prefix1[kMaxExperts + 1];   // tile prefix of the first (or only) GEMM
+  int prefix2[kMaxExperts + 1];   // tile prefix of L2 in the fused kernel
+  int dense[kMaxExperts + 1];     // prefix of slot counts (dense slot ids)
+  int mtiles[kMaxExperts];
+  int off[kMaxExperts];
+  int cnt[kMaxExperts];
 };
 
 // Tile t -> (expert, n-tile, m-tile); m-tiles vary fastest so that CTAs
@@ -141,6 +162,37 @@ struct WorkIter {
   __device__ int slot(int c, int tile) const { return 2 * c + (tile == first_tile(c) ? 0 : 1); }
 };
 
+// One grouped GEMM as the roles see it.
+struct Phase {
+  const GemmArgs* a;
+  const CUtensorMap* map_a;
+  const CUtensorMap* map_b;
+  const int* prefix;
+  int total_tiles, k_blocks, k_stages, k_atoms;
+};
+
+__device__ __forceinline__ Phase make_phase(const GemmArgs& a, const CUtensorMap* ma,
+                                            const CUtensorMap* mb, const int* prefix, int E) {
+  Phase p;
+  p.a = &a;
+  p.map_a = ma;
+  p.map_b = mb;
+  p.prefix = prefix;
+  p.total_tiles = prefix[E];
+  p.k_blocks = a.K / 64;
+  p.k_stages = (a.K + kStageK - 1) / kStageK;
+  p.k_atoms = p.k_stages * 4;
+  return p;
+}
+
+// Pipeline position of one role (carried across the phases of the fused kernel).
+struct Pipe {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t acc_phase = 0;
+  int issued = 0;
+};
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // L1 epilogue on 32 columns: gate g[] and up u[] (raw accumulators).
@@ -188,41 +240,354 @@ __device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float (&v)[32]) {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-    const GemmArgs args) {
-  extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the 128-byte-swizzled tiles
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
-  __shared__ int s_prefix[kMaxExperts + 1];
-  __shared__ int s_mtiles[kMaxExperts];
-  __shared__ int s_off[kMaxExperts];
-  __shared__ int s_cnt[kMaxExperts];
-  __shared__ float s_amax[4];
-  __shared__ int s_last;
-  __shared__ int s_ok;
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
+// Bounded wait until *flag >= target.  Returns false on timeout (status set).
+__device__ bool wait_flag(const int* flag, int target, int* status, volatile int* abort) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire(flag) < target) {
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_status(status, kErrTimeout);
+      if (abort != nullptr) *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// Grid-wide barrier of a cooperative launch, called by one thread per CTA.
+// bar[0] counts arrivals, bar[1] is the generation; both start at zero
+// (the host clears them before the launch).  Everything this CTA wrote
+// before the call is visible to every CTA after it, to the generic and the
+// async (TMA) proxy.
+__device__ bool grid_barrier(int* bar, int generation, int* status, volatile int* abort) {
+  fence_proxy_async_global();
+  __threadfence();
+  if (atomicAdd(&bar[0], 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(&bar[0], 0);
+    __threadfence();
+    atomicExch(&bar[1], generation);
+    return true;
+  }
+  return wait_flag(&bar[1], generation, status, abort);
+}
+
+// ------------------------------------------------------------ producer --
+// Issues the loads of every stage of this CTA's items.  When `gate` is
+// given, the A-operand (activation) loads wait until *gate >= gate_target:
+// the weight (B) loads of the first stages go out first and the activation
+// loads follow once the gate opens.
+__device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* bars,
+                             uint8_t* smem, Pipe& pp, volatile int* abort, const int* gate,
+                             int gate_target) {
+  const GemmArgs& args = *P.a;
+  WorkIter it;
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  const uint64_t pol_a = policy_evict_last();
+  const uint64_t pol_b = policy_evict_first();
+  bool gate_open = gate == nullptr;
+  // activation loads waiting for the gate: (stage, a_row, ks)
+  int def_stage[kStages], def_row[kStages], def_ks[kStages];
+  int n_def = 0;
+  auto issue_a = [&](int stage, int a_row, int ks) {
+    uint64_t* full = &bars->full[stage];
+    tma_load_2d(smem + kOffA + stage * kABytes, P.map_a, ks * kRowBytes, a_row, full, pol_a);
+    const uint8_t* sfa = args.a_sf +
+                         (static_cast<size_t>(a_row / 128) * P.k_atoms + ks * 4) * kSfAtomBytes;
+    bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa, kSfaBytes, full, pol_a);
+  };
+  auto open_gate = [&]() -> bool {
+    // while waiting, pull more of this CTA's weights into L2
+    WorkIter peek = it;
+    int tile, s0, s1, n = 0;
+    while (n < kGatePrefetchStages && peek.next(tile, s0, s1)) {
+      const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
+      const int b_row0 = ti.e * args.N + ti.nt * kBN;
+      for (int ks = s0; ks < s1 && n < kGatePrefetchStages; ++ks, ++n) {
+        tma_prefetch_3d(P.map_b, 0, 0, (b_row0 / 128) * P.k_stages + ks);
+        tma_prefetch_3d(P.map_b, 0, 0, (b_row0 / 128 + 1) * P.k_stages + ks);
+      }
+    }
+    if (!wait_flag(gate, gate_target, args.status, abort)) return false;
+    gate_open = true;
+    for (int i = 0; i < n_def; ++i) issue_a(def_stage[i], def_row[i], def_ks[i]);
+    n_def = 0;
+    return true;
+  };
+  bool ok = true;
+  int tile, s0, s1;
+  while (ok && it.next(tile, s0, s1)) {
+    const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
+    const int a_row = tb.off[ti.e] + ti.mt * kBM;
+    int b_row0, b_row1;
+    if (args.mode == 1) {
+      b_row0 = ti.e * args.N + ti.nt * 128;
+      b_row1 = b_row0 + args.I;
+    } else {
+      b_row0 = ti.e * args.N + ti.nt * kBN;
+      b_row1 = b_row0 + 128;
+    }
+    // B is stored as contiguous 16 KB tiles (128 rows x one K-stage)
+    const int b_tile0 = (b_row0 / 128) * P.k_stages;
+    const int b_tile1 = (b_row1 / 128) * P.k_stages;
+    const uint8_t* sfb0 = args.b_sf + (static_cast<size_t>(b_row0 / 128) * P.k_atoms) * kSfAtomBytes;
+    const uint8_t* sfb1 = args.b_sf + (static_cast<size_t>(b_row1 / 128) * P.k_atoms) * kSfAtomBytes;
+    for (int ks = s0; ks < s1; ++ks) {
+      if (!gate_open && n_def == kStages && !open_gate()) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(&bars->empty[pp.stage], pp.phase ^ 1u, args.status, abort)) {
+        ok = false;
+        break;
+      }
+      const int stage = pp.stage;
+      uint64_t* full = &bars->full[stage];
+      mbar_arrive_expect_tx(full, kStageTx);
+      tma_load_3d(smem + kOffB + stage * kBBytes, P.map_b, 0, 0, b_tile0 + ks, full, pol_b);
+      tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, P.map_b, 0, 0, b_tile1 + ks,
+                  full, pol_b);
+      const size_t koff = static_cast<size_t>(ks) * 4 * kSfAtomBytes;
+      bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb0 + koff, kSfaBytes, full, pol_b);
+      bulk_load(smem + kOffSfb + stage * kSfbBytes + kSfaBytes, sfb1 + koff, kSfaBytes, full,
+                pol_b);
+      if (gate_open) {
+        issue_a(stage, a_row, ks);
+      } else {
+        def_stage[n_def] = stage;
+        def_row[n_def] = a_row;
+        def_ks[n_def] = ks;
+        ++n_def;
+      }
+      ++pp.issued;
+      if (++pp.stage == kStages) {
+        pp.stage = 0;
+        pp.phase ^= 1u;
+      }
+    }
+  }
+  if (ok && !gate_open && n_def > 0) ok = open_gate();
+  return ok;
+}
+
+// Wait (bounded) for the last loads issued so that no copy into this CTA's
+// shared memory is in flight when it exits.
+__device__ void drain_producer(Barriers* bars, Pipe& pp, int* status) {
+  const int tail = pp.issued < kStages ? pp.issued : kStages;
+  int stage = pp.stage;
+  uint32_t phase = pp.phase;
+  for (int i = 0; i < tail; ++i) {
+    if (--stage < 0) {
+      stage = kStages - 1;
+      phase ^= 1u;
+    }
+    mbar_wait(&bars->full[stage], phase, status, nullptr);
+  }
+}
+
+// ----------------------------------------------------------------- MMA --
+__device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t tmem, Pipe& pp,
+                        volatile int* abort) {
+  const GemmArgs& args = *P.a;
+  WorkIter it;
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  const uint32_t idesc = idesc_mxf4nvf4(kBM, kBN);
+  int tile, s0, s1;
+  while (it.next(tile, s0, s1)) {
+    if (!mbar_wait(&bars->acc_empty, pp.acc_phase ^ 1u, args.status, abort)) return false;
+    tc_fence_after();
+    for (int ks = s0; ks < s1; ++ks) {
+      if (!mbar_wait(&bars->full[pp.stage], pp.phase, args.status, abort)) return false;
+      tc_fence_after();
+      const int stage = pp.stage;
+      const uint32_t sfa_t = tmem + kTmemSf + stage * kTmemSfStage;
+      const uint32_t sfb_t = sfa_t + 16;
+      const uint32_t a_base = smem_u32(smem + kOffA + stage * kABytes);
+      const uint32_t b_base = smem_u32(smem + kOffB + stage * kBBytes);
+      const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+      const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
+      const int nkb = min(4, P.k_blocks - ks * 4);
+      for (int kb = 0; kb < nkb; ++kb) {
+        tmem_cp_32x128b_warpx4(sfa_t + kb * 4, smem_desc(sfa_s + kb * kSfAtomBytes, 16, 128, 0));
+        tmem_cp_32x128b_warpx4(sfb_t + kb * 8, smem_desc(sfb_s + kb * kSfAtomBytes, 16, 128, 0));
+        tmem_cp_32x128b_warpx4(sfb_t + kb * 8 + 4,
+                               smem_desc(sfb_s + kSfaBytes + kb * kSfAtomBytes, 16, 128, 0));
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        const uint64_t adesc = smem_desc(a_base + kb * 32, 16, 1024, 2);
+        const uint64_t bdesc = smem_desc(b_base + kb * 32, 16, 1024, 2);
+        mma_mxf4nvf4(tmem, adesc, bdesc, idesc, sfa_t + kb * 4, sfb_t + kb * 8,
+                     (ks != s0 || kb != 0) ? 1u : 0u);
+      }
+      tc_commit(&bars->empty[stage]);
+      if (++pp.stage == kStages) {
+        pp.stage = 0;
+        pp.phase ^= 1u;
+      }
+    }
+    tc_commit(&bars->acc_full);
+    pp.acc_phase ^= 1u;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------ epilogue --
+// Four warps (128 threads, one accumulator row each).  Returns false when
+// a wait gave up; the decision is shared so all four warps leave together.
+__device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* bars,
+                             uint32_t tmem, Pipe& pp, volatile int* abort, float& amax,
+                             int* s_ok, int* s_last) {
+  const GemmArgs& args = *P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = args.E;
+  const int q = warp & 3;                      // TMEM lane quarter
+  const int row_in_tile = q * 32 + lane;
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const bool lead = warp == 2 && lane == 0;
+  WorkIter it;
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  const float gs_a = __ldcg(args.gs_a);
+  int tile, s0, s1;
+  while (it.next(tile, s0, s1)) {
+    const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
+    const float alpha = __fmul_rn(gs_a, args.gs_b[ti.e]);
+    // one thread waits (bounded) and the decision is shared, so the four
+    // epilogue warps always take the same path through the named barriers
+    if (lead) *s_ok = mbar_wait(&bars->acc_full, pp.acc_phase, args.status, abort) ? 1 : 0;
+    epi_bar();
+    if (!*s_ok) return false;
+    tc_fence_after();
+    const bool valid = ti.mt * kBM + row_in_tile < tb.cnt[ti.e];
+    const int64_t row = tb.off[ti.e] + ti.mt * kBM + row_in_tile;
+    const int col0 = ti.nt * (args.mode == 1 ? 128 : kBN);
+    if (s0 == 0 && s1 == P.k_stages) {
+      // whole tile in this CTA: epilogue straight from TMEM
+      if (args.mode == 1) {
+        for (int c = 0; c < 4; ++c) {
+          float g[32], u[32];
+          tmem_ld_f32(t_row + c * 32, g);
+          tmem_ld_f32(t_row + 128 + c * 32, u);
+          if (valid) epi_l1(g, u, alpha, row, col0 + c * 32, args, amax);
+        }
+      } else {
+        for (int c = 0; c < 8; ++c) {
+          float a[32];
+          tmem_ld_f32(t_row + c * 32, a);
+          if (valid) epi_l2(a, alpha, row, col0 + c * 32, args);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty);
+    } else {
+      // a piece of a split tile: park the raw accumulator in the workspace
+      float* mine = args.partials +
+                    (static_cast<size_t>(it.slot(blockIdx.x, tile)) * kBM + row_in_tile) * kBN;
+      for (int c = 0; c < 8; ++c) {
+        float a[32];
+        tmem_ld_f32(t_row + c * 32, a);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            __stcg(reinterpret_cast<float4*>(mine + c * 32 + i),
+                   make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty);
+      __threadfence();
+      epi_bar();
+      const int64_t u_first = static_cast<int64_t>(tile) * P.k_stages;
+      const int c_first = it.owner(u_first);
+      const int c_last = it.owner(u_first + P.k_stages - 1);
+      if (lead) *s_last = atomicAdd(&args.counters[tile], 1) == c_last - c_first;
+      epi_bar();
+      if (*s_last) {
+        // every piece has landed: sum them in ascending K order
+        __threadfence();
+        if (lead) args.counters[tile] = 0;
+        if (valid) {
+          const int nch = args.mode == 1 ? 4 : 8;
+          for (int c = 0; c < nch; ++c) {
+            float a[32], b[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.0f;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const float* p = args.partials +
+                               (static_cast<size_t>(it.slot(cc, tile)) * kBM + row_in_tile) * kBN;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(p + c * 32 + i));
+                a[i] += v.x; a[i + 1] += v.y; a[i + 2] += v.z; a[i + 3] += v.w;
+                if (args.mode == 1) {
+                  const float4 w = __ldcg(reinterpret_cast<const float4*>(p + 128 + c * 32 + i));
+                  b[i] += w.x; b[i + 1] += w.y; b[i + 2] += w.z; b[i + 3] += w.w;
+                }
+              }
+            }
+            if (args.mode == 1)
+              epi_l1(a, b, alpha, row, col0 + c * 32, args, amax);
+            else
+              epi_l2(a, alpha, row, col0 + c * 32, args);
+          }
+        }
+      }
+    }
+    pp.acc_phase ^= 1u;
+  }
+  return true;
+}
 
+// Per-CTA amax of the L1 epilogue -> amax_partial[blockIdx.x] (epilogue warps).
+__device__ void publish_amax(float amax, float* s_amax, float* out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  amax = warp_max(amax);
+  if (lane == 0) s_amax[warp & 3] = amax;
+  epi_bar();
+  if (warp == 2 && lane == 0)
+    out[blockIdx.x] = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
+}
+
+// ---------------------------------------------------------- kernel set-up --
+__device__ void load_tables(Tables& tb, const GemmArgs& a1, int n_tiles2) {
+  const int E = a1.E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int c = args.expert_counts[e];
-    s_cnt[e] = c;
-    s_off[e] = args.expert_offsets[e];
-    s_mtiles[e] = (c + kBM - 1) / kBM;
+    const int c = a1.expert_counts[e];
+    tb.cnt[e] = c;
+    tb.off[e] = a1.expert_offsets[e];
+    tb.mtiles[e] = (c + kBM - 1) / kBM;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int acc = 0;
+    int p1 = 0, p2 = 0, d = 0;
     for (int e = 0; e < E; ++e) {
-      s_prefix[e] = acc;
-      acc += s_mtiles[e] * args.n_tiles;
+      tb.prefix1[e] = p1;
+      tb.prefix2[e] = p2;
+      tb.dense[e] = d;
+      p1 += tb.mtiles[e] * a1.n_tiles;
+      p2 += tb.mtiles[e] * n_tiles2;
+      d += tb.cnt[e];
     }
-    s_prefix[E] = acc;
+    tb.prefix1[E] = p1;
+    tb.prefix2[E] = p2;
+    tb.dense[E] = d;
   }
+}
+
+__device__ uint32_t setup_cta(Barriers* bars, const CUtensorMap* m0, const CUtensorMap* m1,
+                              const CUtensorMap* m2, const CUtensorMap* m3) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -233,8 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbarrier_init();
-    prefetch_tensormap(&map_a);
-    prefetch_tensormap(&map_b);
+    prefetch_tensormap(m0);
+    prefetch_tensormap(m1);
+    if (m2 != nullptr) prefetch_tensormap(m2);
+    if (m3 != nullptr) prefetch_tensormap(m3);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -243,242 +610,177 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-  const int total_tiles = s_prefix[E];
-  volatile int* abort = &bars->abort;
-  const int k_blocks = args.K / 64;
-  const int k_stages = (args.K + kStageK - 1) / kStageK;
-  const int k_atoms = k_stages * 4;
-  WorkIter it;
-  it.init(total_tiles, k_stages, gridDim.x, blockIdx.x);
-  int tile, s0, s1;
+  return bars->tmem_base;
+}
 
-  if (warp == 0) {
-    // ------------------------------------------------------- producer --
-    if (lane == 0) {
-      const uint64_t pol_a = policy_evict_last();
-      const uint64_t pol_b = policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      bool ok = true;
-      while (ok && it.next(tile, s0, s1)) {
-        const TileInfo ti = decode_tile(tile, s_prefix, s_mtiles, E);
-        const int a_row = s_off[ti.e] + ti.mt * kBM;
-        int b_row0, b_row1;
-        if (args.mode == 1) {
-          b_row0 = ti.e * args.N + ti.nt * 128;
-          b_row1 = b_row0 + args.I;
-        } else {
-          b_row0 = ti.e * args.N + ti.nt * kBN;
-          b_row1 = b_row0 + 128;
-        }
-        // B is stored as contiguous 16 KB tiles (128 rows x one K-stage)
-        const int b_tile0 = (b_row0 / 128) * k_stages;
-        const int b_tile1 = (b_row1 / 128) * k_stages;
-        const uint8_t* sfa = args.a_sf + (static_cast<size_t>(a_row / 128) * k_atoms) * kSfAtomBytes;
-        const uint8_t* sfb0 = args.b_sf + (static_cast<size_t>(b_row0 / 128) * k_atoms) * kSfAtomBytes;
-        const uint8_t* sfb1 = args.b_sf + (static_cast<size_t>(b_row1 / 128) * k_atoms) * kSfAtomBytes;
-        for (int ks = s0; ks < s1; ++ks) {
-          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, args.status, abort)) {
-            ok = false;
-            break;
-          }
-          uint64_t* full = &bars->full[stage];
-          mbar_arrive_expect_tx(full, kStageTx);
-          const int32_t x = ks * kRowBytes;
-          tma_load_2d(smem + kOffA + stage * kABytes, &map_a, x, a_row, full, pol_a);
-          tma_load_3d(smem + kOffB + stage * kBBytes, &map_b, 0, 0, b_tile0 + ks, full, pol_b);
-          tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, 0, 0, b_tile1 + ks,
-                      full, pol_b);
-          const size_t koff = static_cast<size_t>(ks) * 4 * kSfAtomBytes;
-          bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + koff, kSfaBytes, full, pol_a);
-          bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb0 + koff, kSfaBytes, full, pol_b);
-          bulk_load(smem + kOffSfb + stage * kSfbBytes + kSfaBytes, sfb1 + koff, kSfaBytes, full,
-                    pol_b);
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // Wait (bounded) for the last loads issued so that no copy into this
-      // CTA's shared memory is in flight when it exits.
-      const int tail = issued < kStages ? issued : kStages;
-      for (int i = 0; i < tail; ++i) {
-        if (--stage < 0) {
-          stage = kStages - 1;
-          phase ^= 1u;
-        }
-        mbar_wait(&bars->full[stage], phase, args.status, nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA --
-    if (lane == 0) {
-      const uint32_t idesc = idesc_mxf4nvf4(kBM, kBN);
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      while (ok && it.next(tile, s0, s1)) {
-        if (!mbar_wait(&bars->acc_empty, acc_phase ^ 1u, args.status, abort)) break;
-        tc_fence_after();
-        for (int ks = s0; ks < s1; ++ks) {
-          if (!mbar_wait(&bars->full[stage], phase, args.status, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sfa_t = tmem + kTmemSf + stage * kTmemSfStage;
-          const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t a_base = smem_u32(smem + kOffA + stage * kABytes);
-          const uint32_t b_base = smem_u32(smem + kOffB + stage * kBBytes);
-          const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
-          const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
-          const int nkb = min(4, k_blocks - ks * 4);
-          for (int kb = 0; kb < nkb; ++kb) {
-            tmem_cp_32x128b_warpx4(sfa_t + kb * 4, smem_desc(sfa_s + kb * kSfAtomBytes, 16, 128, 0));
-            tmem_cp_32x128b_warpx4(sfb_t + kb * 8, smem_desc(sfb_s + kb * kSfAtomBytes, 16, 128, 0));
-            tmem_cp_32x128b_warpx4(sfb_t + kb * 8 + 4,
-                                   smem_desc(sfb_s + kSfaBytes + kb * kSfAtomBytes, 16, 128, 0));
-          }
-          for (int kb = 0; kb < nkb; ++kb) {
-            const uint64_t adesc = smem_desc(a_base + kb * 32, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(b_base + kb * 32, 16, 1024, 2);
-            mma_mxf4nvf4(tmem, adesc, bdesc, idesc, sfa_t + kb * 4, sfb_t + kb * 8,
-                         (ks != s0 || kb != 0) ? 1u : 0u);
-          }
-          tc_commit(&bars->empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(&bars->acc_full);
-        acc_phase ^= 1u;
-      }
-      // make sure every MMA issued by this thread has finished before TMEM
-      // is released
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, args.status, nullptr);
-    }
-  } else {
-    // ------------------------------------------------------- epilogue --
-    const int q = warp & 3;                      // TMEM lane quarter
-    const int row_in_tile = q * 32 + lane;
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const bool lead = warp == 2 && lane == 0;
-    float amax = 0.0f;
-    uint32_t acc_phase = 0;
-    const float gs_a = *args.gs_a;
-    while (it.next(tile, s0, s1)) {
-      const TileInfo ti = decode_tile(tile, s_prefix, s_mtiles, E);
-      const float alpha = __fmul_rn(gs_a, args.gs_b[ti.e]);
-      // one thread waits (bounded) and the decision is shared, so the four
-      // epilogue warps always take the same path through the named barriers
-      if (lead) s_ok = mbar_wait(&bars->acc_full, acc_phase, args.status, abort) ? 1 : 0;
-      epi_bar();
-      if (!s_ok) break;
-      tc_fence_after();
-      const bool valid = ti.mt * kBM + row_in_tile < s_cnt[ti.e];
-      const int64_t row = s_off[ti.e] + ti.mt * kBM + row_in_tile;
-      const int col0 = ti.nt * (args.mode == 1 ? 128 : kBN);
-      if (s0 == 0 && s1 == k_stages) {
-        // whole tile in this CTA: epilogue straight from TMEM
-        if (args.mode == 1) {
-          for (int c = 0; c < 4; ++c) {
-            float g[32], u[32];
-            tmem_ld_f32(t_row + c * 32, g);
-            tmem_ld_f32(t_row + 128 + c * 32, u);
-            if (valid) epi_l1(g, u, alpha, row, col0 + c * 32, args, amax);
-          }
-        } else {
-          for (int c = 0; c < 8; ++c) {
-            float a[32];
-            tmem_ld_f32(t_row + c * 32, a);
-            if (valid) epi_l2(a, alpha, row, col0 + c * 32, args);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->acc_empty);
-      } else {
-        // a piece of a split tile: park the raw accumulator in the workspace
-        float* mine = args.partials +
-                      (static_cast<size_t>(it.slot(blockIdx.x, tile)) * kBM + row_in_tile) * kBN;
-        for (int c = 0; c < 8; ++c) {
-          float a[32];
-          tmem_ld_f32(t_row + c * 32, a);
-          if (valid) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              __stcg(reinterpret_cast<float4*>(mine + c * 32 + i),
-                     make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]));
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->acc_empty);
-        __threadfence();
-        epi_bar();
-        const int64_t u_first = static_cast<int64_t>(tile) * k_stages;
-        const int c_first = it.owner(u_first);
-        const int c_last = it.owner(u_first + k_stages - 1);
-        if (lead) s_last = atomicAdd(&args.counters[tile], 1) == c_last - c_first;
-        epi_bar();
-        if (s_last) {
-          // every piece has landed: sum them in ascending K order
-          __threadfence();
-          if (lead) args.counters[tile] = 0;
-          if (valid) {
-            const int nch = args.mode == 1 ? 4 : 8;
-            for (int c = 0; c < nch; ++c) {
-              float a[32], b[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.0f;
-              for (int cc = c_first; cc <= c_last; ++cc) {
-                const float* p = args.partials +
-                                 (static_cast<size_t>(it.slot(cc, tile)) * kBM + row_in_tile) * kBN;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(p + c * 32 + i));
-                  a[i] += v.x; a[i + 1] += v.y; a[i + 2] += v.z; a[i + 3] += v.w;
-                  if (args.mode == 1) {
-                    const float4 w = __ldcg(reinterpret_cast<const float4*>(p + 128 + c * 32 + i));
-                    b[i] += w.x; b[i + 1] += w.y; b[i + 2] += w.z; b[i + 3] += w.w;
-                  }
-                }
-              }
-              if (args.mode == 1)
-                epi_l1(a, b, alpha, row, col0 + c * 32, args, amax);
-              else
-                epi_l2(a, alpha, row, col0 + c * 32, args);
-            }
-          }
-        }
-      }
-      acc_phase ^= 1u;
-    }
-    if (args.mode == 1) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-      if (lane == 0) s_amax[q] = amax;
-      epi_bar();
-      if (lead)
-        args.amax_partial[blockIdx.x] =
-            fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
-    }
-  }
-
+// The MMA thread makes sure every MMA it issued has finished; then the
+// allocating warp releases TMEM.
+__device__ void teardown_cta(Barriers* bars, uint32_t tmem) {
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if ((threadIdx.x >> 5) == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
+
+__device__ void mma_drain(Barriers* bars, int* status) {
+  tc_commit(&bars->drain);
+  mbar_wait(&bars->drain, 0, status, nullptr);
+}
+
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+  const uint32_t a = smem_u32(raw);
+  return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// ------------------------------------------------------------- kernels --
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+  __shared__ Tables tb;
+  __shared__ float s_amax[4];
+  __shared__ int s_last, s_ok;
+
+  load_tables(tb, args, args.n_tiles);
+  const uint32_t tmem = setup_cta(bars, &map_a, &map_b, nullptr, nullptr);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &bars->abort;
+  const Phase P = make_phase(args, &map_a, &map_b, tb.prefix1, args.E);
+  Pipe pp;
+  if (warp == 0) {
+    if (lane == 0) {
+      run_producer(P, args.E, tb, bars, smem, pp, abort, nullptr, 0);
+      drain_producer(bars, pp, args.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      run_mma(P, bars, smem, tmem, pp, abort);
+      mma_drain(bars, args.status);
+    }
+  } else {
+    float amax = 0.0f;
+    run_epilogue(P, args.E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    if (args.mode == 1) publish_amax(amax, s_amax, args.amax_partial);
+  }
+  teardown_cta(bars, tmem);
+}
+
+struct FusedArgs {
+  int* grid_bar;          // [2] arrival count, generation; zero at launch
+  const int32_t* row_token;
+  uint8_t* hq;            // [rows, I/2]
+  uint8_t* hsf;           // staged scales of hq
+  float* gs_h;            // [1]
+};
+
+// Requantise h over the valid rows (epilogue warps of every CTA).  The
+// 16-element blocks of all valid rows are spread over the grid, 32 per warp
+// per step; each warp gathers 4 scale bytes into one staged 32-bit word.
+__device__ void requantise(const GemmArgs& a1, const FusedArgs& f, const Tables& tb, int E,
+                           float gs) {
+  const int I = a1.I;
+  const int bpr = I >> 4;
+  const int k_atoms = static_cast<int>((I + kStageK - 1) / kStageK) * 4;
+  const float denom = __fmul_rn(6.0f, gs);
+  const int64_t total = static_cast<int64_t>(tb.dense[E]) * bpr;
+  const int lane = threadIdx.x & 31;
+  const int ew = (threadIdx.x >> 5) - 2;                     // 0..3
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * 128;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * 128 + ew * 32; base < total;
+       base += stride) {
+    const int64_t i = base + lane;
+    const bool active = i < total;
+    const int s = active ? static_cast<int>(i / bpr) : 0;
+    const int g = active ? static_cast<int>(i - static_cast<int64_t>(s) * bpr) : 0;
+    int e = 0;
+    while (e + 1 < E && tb.dense[e + 1] <= s) ++e;
+    const int64_t row = tb.off[e] + (s - tb.dense[e]);
+    float v[16];
+    if (active) {
+      const float* src = a1.out + row * I + g * 16;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(src) + c);
+        v[4 * c] = t.x; v[4 * c + 1] = t.y; v[4 * c + 2] = t.z; v[4 * c + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+    }
+    uint32_t packed[2];
+    const uint32_t sf = quant_block16(v, gs, denom, packed);
+    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sf, 1);
+    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sf, 2);
+    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sf, 3);
+    if (!active) continue;
+    *reinterpret_cast<uint2*>(f.hq + row * (I >> 1) + g * 8) = make_uint2(packed[0], packed[1]);
+    if ((g & 3) == 0)
+      *reinterpret_cast<uint32_t*>(f.hsf + staged_offset(row, g, k_atoms)) =
+          sf | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
+    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w1,
+    const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w2,
+    const GemmArgs a1, const GemmArgs a2, const FusedArgs f) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+  __shared__ Tables tb;
+  __shared__ float s_amax[4];
+  __shared__ int s_last, s_ok;
+
+  load_tables(tb, a1, a2.n_tiles);
+  const uint32_t tmem = setup_cta(bars, &map_x, &map_w1, &map_h, &map_w2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &bars->abort;
+  const int E = a1.E;
+  const Phase P1 = make_phase(a1, &map_x, &map_w1, tb.prefix1, E);
+  const Phase P2 = make_phase(a2, &map_h, &map_w2, tb.prefix2, E);
+  Pipe pp;
+  if (warp == 0) {
+    if (lane == 0) {
+      if (run_producer(P1, E, tb, bars, smem, pp, abort, nullptr, 0))
+        run_producer(P2, E, tb, bars, smem, pp, abort, &f.grid_bar[1], 2);
+      drain_producer(bars, pp, a1.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (run_mma(P1, bars, smem, tmem, pp, abort)) run_mma(P2, bars, smem, tmem, pp, abort);
+      mma_drain(bars, a1.status);
+    }
+  } else {
+    float amax = 0.0f;
+    bool ok = run_epilogue(P1, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    publish_amax(amax, s_amax, a1.amax_partial);
+    // barrier 1: every h row and every per-CTA amax is written
+    if (warp == 2 && lane == 0)
+      s_ok = ok && grid_barrier(f.grid_bar, 1, a1.status, abort) ? 1 : 0;
+    epi_bar();
+    ok = s_ok != 0;
+    if (ok) {
+      const float gs = global_scale_from(reduce_partials(a1.amax_partial, gridDim.x));
+      if (blockIdx.x == 0 && warp == 2 && lane == 0) *f.gs_h = gs;
+      requantise(a1, f, tb, E, gs);
+      epi_bar();
+      // barrier 2: hq, its scales and gs_h are written (opens the producer's
+      // activation loads of L2)
+      if (warp == 2 && lane == 0) s_ok = grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
+      epi_bar();
+      ok = s_ok != 0;
+    }
+    if (ok) run_epilogue(P2, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+  }
+  teardown_cta(bars, tmem);
+}
+
+bool g_gemm_attr = false;
+bool g_fused_attr = false;
 
 }  // namespace
 
@@ -486,16 +788,43 @@ int gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& args, const CUtensorMap& map_a, const CUtensorMap& map_b,
                         int grid, cudaStream_t stream) {
-  static bool attr_set = false;  // per-process; the attribute is per function
-  if (!attr_set) {
+  if (!g_gemm_attr) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    g_gemm_attr = true;
   }
   grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, args);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const CUtensorMap& map_x,
+                             const CUtensorMap& map_w1, const CUtensorMap& map_h,
+                             const CUtensorMap& map_w2, int* grid_bar, const int32_t* row_token,
+                             uint8_t* hq, uint8_t* hsf, float* gs_h, int grid,
+                             cudaStream_t stream) {
+  if (!g_fused_attr) {
+    cudaError_t err = cudaFuncSetAttribute(fused_ffn_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+    if (err != cudaSuccess) return err;
+    g_fused_attr = true;
+  }
+  cudaError_t err = cudaMemsetAsync(grid_bar, 0, 2 * sizeof(int), stream);
+  if (err != cudaSuccess) return err;
+  FusedArgs f{grid_bar, row_token, hq, hsf, gs_h};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_ffn_kernel, map_x, map_w1, map_h, map_w2, a1, a2, f);
 }
 
 }  // namespace nvmoe

@@ -11,10 +11,10 @@
 // (no atomics, no memset) and streams the quantisation with 16-byte loads,
 // one thread per 16-element block.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace nvmoe {
 
@@ -49,12 +49,6 @@ struct Vec<float> {
   }
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kAmaxThreads) quant_amax_kernel(const T* __restrict__ x,
                                                                    int64_t n_vec,
@@ -77,44 +71,6 @@ __global__ void __launch_bounds__(kAmaxThreads) quant_amax_kernel(const T* __res
     r = warp_max(r);
     if (threadIdx.x == 0) partial[blockIdx.x] = r;
   }
-}
-
-// Quantise one 16-element block given gs and denom = 6*gs.
-// Returns the scale byte; `packed` receives 8 bytes (2 nibbles each).
-__device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float gs, float denom,
-                                                  uint32_t (&packed)[2]) {
-  float b = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(v[i]));
-  const uint32_t sf = cvt_e4m3_satfinite(__fdiv_rn(b, denom));
-  const float d = __fmul_rn(e4m3_to_float(sf), gs);
-  packed[0] = packed[1] = 0u;
-  if (d != 0.0f) {
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const float lo = v[2 * p], hi = v[2 * p + 1];
-      uint32_t byte = cvt_e2m1x2_satfinite(__fdiv_rn(fabsf(lo), d), __fdiv_rn(fabsf(hi), d));
-      byte |= (__float_as_uint(lo) >> 31) << 3;
-      byte |= (__float_as_uint(hi) >> 31) << 7;
-      packed[p >> 2] |= byte << (8 * (p & 3));
-    }
-  }
-  return sf;
-}
-
-__device__ __forceinline__ float global_scale_from(float amax) {
-  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
-}
-
-__device__ __forceinline__ float reduce_partials(const float* __restrict__ partial, int n) {
-  float m = 0.0f;
-  for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, partial[i]);
-  return warp_max(m);
-}
-
-__device__ __forceinline__ size_t staged_offset(int64_t row, int g, int k_atoms) {
-  return (static_cast<size_t>(row / kTileRows) * k_atoms + (g >> 2)) * kSfAtomBytes +
-         (row & 31) * 16 + ((row & 127) >> 5) * 4 + (g & 3);
 }
 
 template <typename T>
