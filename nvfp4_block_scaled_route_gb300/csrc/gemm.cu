@@ -60,7 +60,6 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kTmemSfStage = 48;
-constexpr int kGatePrefetchStages = 16;   // fused kernel: L2 weights prefetched while gated
 
 struct __align__(8) Barriers {
   uint64_t full[kStages];
@@ -230,6 +229,43 @@ __device__ __forceinline__ void epi_l2(const float (&a)[32], float alpha, int64_
                     __fmul_rn(alpha, a[i + 2]), __fmul_rn(alpha, a[i + 3]));
 }
 
+// The same epilogues on 4 columns (used by the split-tile fixup, where the
+// 128 epilogue threads share the valid rows' columns).
+__device__ __forceinline__ void epi_l1_4(float4 g, float4 u, float alpha, int64_t row, int col,
+                                         const GemmArgs& args, float& amax) {
+  const int I = args.I;
+  const float gv[4] = {__fmul_rn(alpha, g.x), __fmul_rn(alpha, g.y), __fmul_rn(alpha, g.z),
+                       __fmul_rn(alpha, g.w)};
+  const float uv[4] = {__fmul_rn(alpha, u.x), __fmul_rn(alpha, u.y), __fmul_rn(alpha, u.z),
+                       __fmul_rn(alpha, u.w)};
+  float hv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    hv[j] = __fmul_rn(silu_f(gv[j]), uv[j]);
+    amax = fmaxf(amax, fabsf(hv[j]));
+  }
+  *reinterpret_cast<float4*>(args.out + row * I + col) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+  if (args.tap != nullptr) {
+    float* tp = args.tap + row * (2 * I) + col;
+    *reinterpret_cast<float4*>(tp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+    *reinterpret_cast<float4*>(tp + I) = make_float4(uv[0], uv[1], uv[2], uv[3]);
+  }
+}
+
+__device__ __forceinline__ void epi_l2_4(float4 a, float alpha, int64_t row, int col,
+                                         const GemmArgs& args) {
+  *reinterpret_cast<float4*>(args.out + row * args.N + col) =
+      make_float4(__fmul_rn(alpha, a.x), __fmul_rn(alpha, a.y), __fmul_rn(alpha, a.z),
+                  __fmul_rn(alpha, a.w));
+}
+
+__device__ __forceinline__ void add4(float4& a, float4 b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
 __device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
@@ -308,17 +344,6 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
     bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa, kSfaBytes, full, pol_a);
   };
   auto open_gate = [&]() -> bool {
-    // while waiting, pull more of this CTA's weights into L2
-    WorkIter peek = it;
-    int tile, s0, s1, n = 0;
-    while (n < kGatePrefetchStages && peek.next(tile, s0, s1)) {
-      const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
-      const int b_row0 = ti.e * args.N + ti.nt * kBN;
-      for (int ks = s0; ks < s1 && n < kGatePrefetchStages; ++ks, ++n) {
-        tma_prefetch_3d(P.map_b, 0, 0, (b_row0 / 128) * P.k_stages + ks);
-        tma_prefetch_3d(P.map_b, 0, 0, (b_row0 / 128 + 1) * P.k_stages + ks);
-      }
-    }
     if (!wait_flag(gate, gate_target, args.status, abort)) return false;
     gate_open = true;
     for (int i = 0; i < n_def; ++i) issue_a(def_stage[i], def_row[i], def_ks[i]);
@@ -514,33 +539,43 @@ __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* 
       if (lead) *s_last = atomicAdd(&args.counters[tile], 1) == c_last - c_first;
       epi_bar();
       if (*s_last) {
-        // every piece has landed: sum them in ascending K order
+        // every piece has landed: sum them in ascending K order.  The valid
+        // rows' 4-column groups are spread over all 128 epilogue threads and
+        // the pieces are loaded four at a time, so the fixup is not a chain
+        // of dependent L2 round trips on the few threads that own rows.
         __threadfence();
         if (lead) args.counters[tile] = 0;
-        if (valid) {
-          const int nch = args.mode == 1 ? 4 : 8;
-          for (int c = 0; c < nch; ++c) {
-            float a[32], b[32];
+        const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
+        const int groups = args.mode == 1 ? 32 : 64;   // float4 groups per row
+        const int etid = threadIdx.x - 64;
+        const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
+        for (int wi = etid; wi < n_valid * groups; wi += 128) {
+          const int r = wi / groups, g4 = wi - r * groups;
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+          for (int cc0 = c_first; cc0 <= c_last; cc0 += 4) {
+            float4 va[4], vb[4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.0f;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const float* p = args.partials +
-                               (static_cast<size_t>(it.slot(cc, tile)) * kBM + row_in_tile) * kBN;
-#pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(p + c * 32 + i));
-                a[i] += v.x; a[i + 1] += v.y; a[i + 2] += v.z; a[i + 3] += v.w;
-                if (args.mode == 1) {
-                  const float4 w = __ldcg(reinterpret_cast<const float4*>(p + 128 + c * 32 + i));
-                  b[i] += w.x; b[i + 1] += w.y; b[i + 2] += w.z; b[i + 3] += w.w;
-                }
+            for (int j = 0; j < 4; ++j) {
+              if (cc0 + j <= c_last) {
+                const float* p = args.partials +
+                                 (static_cast<size_t>(it.slot(cc0 + j, tile)) * kBM + r) * kBN +
+                                 g4 * 4;
+                va[j] = __ldcg(reinterpret_cast<const float4*>(p));
+                if (args.mode == 1) vb[j] = __ldcg(reinterpret_cast<const float4*>(p + 128));
               }
             }
-            if (args.mode == 1)
-              epi_l1(a, b, alpha, row, col0 + c * 32, args, amax);
-            else
-              epi_l2(a, alpha, row, col0 + c * 32, args);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (cc0 + j <= c_last) {
+                add4(a, va[j]);
+                if (args.mode == 1) add4(b, vb[j]);
+              }
+            }
           }
+          if (args.mode == 1)
+            epi_l1_4(a, b, alpha, row0 + r, col0 + g4 * 4, args, amax);
+          else
+            epi_l2_4(a, alpha, row0 + r, col0 + g4 * 4, args);
         }
       }
     }
