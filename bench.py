@@ -4,7 +4,8 @@
 One step = the whole forward pass on one batch of synthetic tokens:
 route -> quantise into the grouped slot layout -> L1 grouped GEMM with fused
 alpha/SiLU*up/amax -> requantise -> L2 grouped GEMM -> weighted reduce
-(8 kernels of libnvfp4moe.so, replayed as one CUDA graph).
+(4 to 8 kernels of libnvfp4moe.so depending on the batch size, replayed as one
+CUDA graph; the library counts its own launches).
 
 Default workload: the one-token decode case (E=48 experts, H=7168, I=3072,
 top-8), whose roofline is HBM bandwidth on the weight + scale bytes of the
@@ -44,7 +45,6 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/sec on 1 GB300; % HBM roofline (decode), % FP4 TC peak (prefill)"
 UNIT = "tokens/s"
 FLUSH_BYTES = 256 << 20            # > 129 MB L2
-KERNELS_PER_STEP = 8               # route 2 + quantise 2 + L1 + requant + L2 + reduce
 FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / BF16 tensor ratio on GB300
 
 
@@ -330,6 +330,12 @@ def main():
         for _ in range(3):
             layer.forward(x, ids, w)
     stream.synchronize()
+    # library kernels per step, counted by the library itself on one eager step
+    n0 = nb.lib().nvmoe_kernel_launch_count()
+    with torch.cuda.stream(stream):
+        layer.forward(x, ids, w)
+    stream.synchronize()
+    kernels_per_step = int(nb.lib().nvmoe_kernel_launch_count() - n0)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         layer.forward(x, ids, w)
@@ -381,7 +387,7 @@ def main():
             stage["l2"].append(evs[2].elapsed_time(evs[3]))
     l1_ms = statistics.mean(stage["l1"])
     # the fused path records events 1..3 together after its single kernel
-    fused = max(statistics.mean(stage["requant"]), statistics.mean(stage["l2"])) < 1e-3
+    fused = max(statistics.mean(stage["requant"]), statistics.mean(stage["l2"])) < 0.01
     decode = cfg.T * cfg.k <= 2048
     if decode and fused:
         fb = l1_bytes + l2_bytes
@@ -453,7 +459,7 @@ def main():
                        "stage_ms": {k: statistics.mean(v) for k, v in stage.items()},
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks,
+            "gpu_launches": kernels_per_step * args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -79,6 +79,11 @@ const char* nvmoe_status_str(int status);
 /* Library ABI version (major * 100 + minor). */
 int nvmoe_version(void);
 
+/* Number of kernels this library has enqueued in this process so far (all
+ * entry points; a replay of a captured CUDA graph enqueues nothing new).
+ * For accounting and tests; no synchronisation. */
+uint64_t nvmoe_kernel_launch_count(void);
+
 /* Read (and optionally clear) the device status word that a workspace
  * carries at its start.  Synchronises `stream`.  `status_out` is a HOST
  * pointer.  Every workspace-taking call writes only nonzero codes there; a

@@ -50,6 +50,7 @@ _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size
 SIGNATURES = {
     "nvmoe_status_str": (ctypes.c_char_p, [_I]),
     "nvmoe_version": (_I, []),
+    "nvmoe_kernel_launch_count": (ctypes.c_uint64, []),
     "nvmoe_read_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "nvmoe_clear_status": (_I, [_P, _P]),
     "nvfp4_sf_mma_bytes": (_SZ, [_I64, _I64]),

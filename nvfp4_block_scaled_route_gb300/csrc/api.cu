@@ -2,6 +2,7 @@
 // argument checks, workspace carving, TMA descriptor encoding and kernel
 // launches.  No allocation, no host synchronisation on the compute calls.
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "nvfp4moe.h"
@@ -76,6 +77,15 @@ int sm_count() {
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? NVMOE_OK : NVMOE_ERR_CUDA; }
 
+// Kernels of this library enqueued so far (CUDA-graph replays are not
+// launches and are not counted).
+std::atomic<uint64_t> g_launches{0};
+
+cudaError_t counted(cudaError_t e, int kernels) {
+  if (e == cudaSuccess) g_launches += kernels;
+  return e;
+}
+
 // Workspace carving helper.
 struct Carve {
   uint8_t* base;
@@ -113,6 +123,8 @@ const char* nvmoe_status_str(int s) {
 }
 
 int nvmoe_version(void) { return 100; }
+
+uint64_t nvmoe_kernel_launch_count(void) { return g_launches.load(); }
 
 int nvmoe_read_status(const void* ws, cudaStream_t stream, int* out) {
   if (ws == nullptr || out == nullptr) return NVMOE_ERR_INVALID_ARG;
@@ -162,9 +174,9 @@ int moe_route_permute(const int32_t* topk_ids, int64_t T, int k, int E, int32_t*
   Carve c{static_cast<uint8_t*>(ws)};
   int* status = c.take<int>(kStatusBytes);
   int32_t* chunk_counts = c.take<int32_t>(static_cast<size_t>(n_chunks) * E * sizeof(int32_t));
-  return status_of(launch_route(topk_ids, T, k, E, expert_offsets, expert_counts, row_token,
+  return status_of(counted(launch_route(topk_ids, T, k, E, expert_offsets, expert_counts, row_token,
                                 rows_bound(T, k, E), slot_of, chunk_counts, n_chunks, status,
-                                stream));
+                                stream), n_chunks == 1 ? 1 : 2));
 }
 
 // --------------------------------------------------------- quantiser ----
@@ -192,11 +204,15 @@ int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
   c.take<int>(kStatusBytes);
   float* partial = c.take<float>(kQuantMaxPartials * sizeof(float));
   const int64_t n = rows * cols;
+  if (n <= kQuantSmallElems)
+    return status_of(counted(launch_quant_small(x, x_dtype, rows, cols, row_dst, fanout, q,
+                                                sf_rowmajor, sf_mma, gs_out, stream), 1));
   const int parts = quant_amax_blocks(n);
-  cudaError_t e = launch_quant_amax(x, x_dtype, n, partial, parts, stream);
+  cudaError_t e = counted(launch_quant_amax(x, x_dtype, n, partial, parts, stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
-  return status_of(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr, partial,
-                                     parts, q, sf_rowmajor, sf_mma, gs_out, stream));
+  return status_of(counted(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr,
+                                             partial, parts, q, sf_rowmajor, sf_mma, gs_out,
+                                             stream), 1));
 }
 
 // ----------------------------------------------------------- weights ----
@@ -219,9 +235,9 @@ int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q, uint
   Carve c{static_cast<uint8_t*>(ws)};
   c.take<int>(kStatusBytes);
   float* partial = c.take<float>(static_cast<size_t>(E) * 64 * sizeof(float));
-  cudaError_t e = launch_weight_amax(w, E, static_cast<int64_t>(K) * N, partial, 64, stream);
+  cudaError_t e = counted(launch_weight_amax(w, E, static_cast<int64_t>(K) * N, partial, 64, stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
-  return status_of(launch_weight_quant(w, E, K, N, partial, 64, q, sf, gs, stream));
+  return status_of(counted(launch_weight_quant(w, E, K, N, partial, 64, q, sf, gs, stream), 1));
 }
 
 size_t moe_nvfp4_prepared_bytes(int E, int K, int N) {
@@ -235,7 +251,7 @@ int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int
       q_out == nullptr || sf_out == nullptr)
     return NVMOE_ERR_INVALID_ARG;
   if (K % 64 != 0 || N % kTileRows != 0 || E > 65535) return NVMOE_ERR_UNSUPPORTED_SHAPE;
-  return status_of(launch_prepare_weights(q_ckpt, sf_ckpt, E, K, N, q_out, sf_out, stream));
+  return status_of(counted(launch_prepare_weights(q_ckpt, sf_ckpt, E, K, N, q_out, sf_out, stream), 2));
 }
 
 // ----------------------------------------------------------- forward ----
@@ -376,8 +392,8 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   if (timed && cudaEventRecord(ev[0], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   if (fused) {
     const int g = grid_for(tiles1 > tiles2 ? tiles1 : tiles2);
-    cudaError_t e = launch_fused_ffn(a1, a2, map_x, map_w1, map_h, map_w2, b.grid_bar, row_token,
-                                     b.hq, b.hsf, b.gs_h, g, stream);
+    cudaError_t e = counted(launch_fused_ffn(a1, a2, map_x, map_w1, map_h, map_w2, b.grid_bar,
+                                             row_token, b.hq, b.hsf, b.gs_h, g, stream), 1);
     if (e != cudaSuccess) return NVMOE_ERR_CUDA;
     if (timed) {
       // one kernel: L1, requantisation and L2 are not separable
@@ -387,15 +403,15 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
     return NVMOE_OK;
   }
   const int g1 = grid_for(tiles1);
-  cudaError_t e = launch_gemm(a1, map_x, map_w1, g1, stream);
+  cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
   if (timed && cudaEventRecord(ev[1], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   // requantise h over the valid rows (global amax from the L1 partials)
-  e = launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1, b.hq, nullptr,
-                        b.hsf, b.gs_h, stream);
+  e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1, b.hq,
+                                nullptr, b.hsf, b.gs_h, stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
   if (timed && cudaEventRecord(ev[2], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
-  e = launch_gemm(a2, map_h, map_w2, grid_for(tiles2), stream);
+  e = counted(launch_gemm(a2, map_h, map_w2, grid_for(tiles2), stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
   if (timed && cudaEventRecord(ev[3], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   return NVMOE_OK;
@@ -412,7 +428,7 @@ int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of, const fl
   if (slot_out == nullptr || slot_of == nullptr || topk_w == nullptr || y == nullptr)
     return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(slot_out) || !aligned16(y)) return NVMOE_ERR_MISALIGNED;
-  return status_of(launch_reduce(slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream));
+  return status_of(counted(launch_reduce(slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream), 1));
 }
 
 }  // extern "C"

@@ -44,6 +44,11 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
                               uint8_t* sf_row, uint8_t* sf_mma, float* gs_out,
                               cudaStream_t stream);
 int quant_amax_blocks(int64_t n_elems);
+// Both passes in one CTA, for inputs of at most kQuantSmallElems elements.
+constexpr int64_t kQuantSmallElems = 64 * 1024;
+cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                               const int32_t* row_dst, int fanout, uint8_t* q, uint8_t* sf_row,
+                               uint8_t* sf_mma, float* gs_out, cudaStream_t stream);
 
 // ---- weights ----
 cudaError_t launch_weight_amax(const float* w, int E, int64_t per_expert, float* partial,

@@ -73,30 +73,20 @@ __global__ void __launch_bounds__(kAmaxThreads) quant_amax_kernel(const T* __res
   }
 }
 
+// Quantise rows of x given gs: one thread per 16-element block, a
+// warp-uniform grid-stride loop so that the shuffles always see all 32 lanes.
 template <typename T>
-__global__ void __launch_bounds__(kPackThreads) quant_pack_kernel(
-    const T* __restrict__ x, int64_t rows, int cols, const int32_t* __restrict__ row_dst,
-    int fanout, const int32_t* __restrict__ row_valid, const float* __restrict__ partial,
-    int n_partial, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
-    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms) {
+__device__ __forceinline__ void pack_rows(const T* __restrict__ x, int64_t rows, int cols,
+                                          const int32_t* __restrict__ row_dst, int fanout,
+                                          const int32_t* __restrict__ row_valid, float gs,
+                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
+                                          uint8_t* __restrict__ sf_mma, int k_atoms) {
   constexpr int VE = Vec<T>::kElems;
-  __shared__ float s_gs;
-  if (threadIdx.x < 32) {
-    const float amax = reduce_partials(partial, n_partial);
-    if (threadIdx.x == 0) {
-      const float gs = global_scale_from(amax);
-      s_gs = gs;
-      if (blockIdx.x == 0 && gs_out != nullptr) *gs_out = gs;
-    }
-  }
-  __syncthreads();
-  const float gs = s_gs;
   const float denom = __fmul_rn(6.0f, gs);
   const int bpr = cols >> 4;                       // blocks per row
   const int64_t total = rows * bpr;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  // warp-uniform loop so that the shuffles below always see all 32 lanes
   for (int64_t base = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); base < total;
        base += stride) {
     const int64_t i = base + lane;
@@ -136,6 +126,59 @@ __global__ void __launch_bounds__(kPackThreads) quant_pack_kernel(
         *reinterpret_cast<uint32_t*>(sf_mma + staged_offset(dst, g, k_atoms)) = word;
     }
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPackThreads) quant_pack_kernel(
+    const T* __restrict__ x, int64_t rows, int cols, const int32_t* __restrict__ row_dst,
+    int fanout, const int32_t* __restrict__ row_valid, const float* __restrict__ partial,
+    int n_partial, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
+    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms) {
+  __shared__ float s_gs;
+  if (threadIdx.x < 32) {
+    const float amax = reduce_partials(partial, n_partial);
+    if (threadIdx.x == 0) {
+      const float gs = global_scale_from(amax);
+      s_gs = gs;
+      if (blockIdx.x == 0 && gs_out != nullptr) *gs_out = gs;
+    }
+  }
+  __syncthreads();
+  pack_rows<T>(x, rows, cols, row_dst, fanout, row_valid, s_gs, q, sf_row, sf_mma, k_atoms);
+}
+
+// Small inputs: amax and quantisation in one CTA (one launch instead of two).
+constexpr int kSmallThreads = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kSmallThreads) quant_small_kernel(
+    const T* __restrict__ x, int64_t rows, int cols, const int32_t* __restrict__ row_dst,
+    int fanout, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
+    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms) {
+  constexpr int VE = Vec<T>::kElems;
+  __shared__ float s_red[kSmallThreads / 32];
+  __shared__ float s_gs;
+  const int64_t n_vec = rows * cols / VE;
+  float m = 0.0f;
+  for (int64_t i = threadIdx.x; i < n_vec; i += blockDim.x) {
+    float v[VE];
+    Vec<T>::load(x + i * VE, v);
+#pragma unroll
+    for (int j = 0; j < VE; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const float r = warp_max(s_red[threadIdx.x]);
+    if (threadIdx.x == 0) {
+      const float gs = global_scale_from(r);
+      s_gs = gs;
+      if (gs_out != nullptr) *gs_out = gs;
+    }
+  }
+  __syncthreads();
+  pack_rows<T>(x, rows, cols, row_dst, fanout, nullptr, s_gs, q, sf_row, sf_mma, k_atoms);
 }
 
 // ------------------------------------------------------------- weights ----
@@ -256,6 +299,21 @@ cudaError_t launch_quant_amax(const void* x, int x_dtype, int64_t n_elems, float
     quant_amax_kernel<float><<<n_partial, kAmaxThreads, 0, stream>>>(
         static_cast<const float*>(x), n_elems / 4, partial);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                               const int32_t* row_dst, int fanout, uint8_t* q, uint8_t* sf_row,
+                               uint8_t* sf_mma, float* gs_out, cudaStream_t stream) {
+  const int k_atoms = static_cast<int>(round_up(cols, kStageK) / 64);
+  if (x_dtype == 0)
+    quant_small_kernel<__nv_bfloat16><<<1, kSmallThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, static_cast<int>(cols), row_dst, fanout, q,
+        sf_row, sf_mma, gs_out, k_atoms);
+  else
+    quant_small_kernel<float><<<1, kSmallThreads, 0, stream>>>(
+        static_cast<const float*>(x), rows, static_cast<int>(cols), row_dst, fanout, q, sf_row,
+        sf_mma, gs_out, k_atoms);
   return cudaGetLastError();
 }
 

@@ -46,20 +46,37 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(
     const int32_t* __restrict__ ids, int64_t S, int k, int E,
     const int32_t* __restrict__ chunk_counts, int n_chunks, int32_t* __restrict__ expert_offsets,
     int32_t* __restrict__ expert_counts, int32_t* __restrict__ row_token,
-    int32_t* __restrict__ slot_of) {
+    int32_t* __restrict__ slot_of, int64_t rows_bound, int* status) {
   __shared__ int base[kMaxExperts];        // first row of this chunk's slots per expert
   __shared__ int total[kMaxExperts];
   __shared__ int whist[kWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int tot = 0, pre = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int v = chunk_counts[static_cast<int64_t>(c) * E + e];
-      tot += v;
-      if (c < static_cast<int>(blockIdx.x)) pre += v;
+  if (chunk_counts == nullptr) {
+    // single CTA (S <= one chunk): histogram here, no counting launch
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      total[e] = 0;
+      base[e] = 0;
     }
-    total[e] = tot;
-    base[e] = pre;
+    for (int64_t r = threadIdx.x; r < rows_bound; r += blockDim.x) row_token[r] = -1;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < S; i += blockDim.x) {
+      const int e = ids[i];
+      if (e >= 0 && e < E)
+        atomicAdd(&total[e], 1);
+      else
+        record_status(status, kErrBadIndex);
+    }
+  } else {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int tot = 0, pre = 0;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int v = chunk_counts[static_cast<int64_t>(c) * E + e];
+        tot += v;
+        if (c < static_cast<int>(blockIdx.x)) pre += v;
+      }
+      total[e] = tot;
+      base[e] = pre;
+    }
   }
   for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += blockDim.x)
     (&whist[0][0])[i] = 0;
@@ -137,13 +154,20 @@ cudaError_t launch_route(const int32_t* topk_ids, int64_t T, int k, int E,
                          int64_t rows_bound, int32_t* slot_of, int32_t* chunk_counts,
                          int n_chunks, int* status, cudaStream_t stream) {
   const int64_t S = T * k;
+  if (n_chunks == 1) {
+    // one chunk: histogram, prefix sum and assignment in a single CTA
+    route_assign_kernel<<<1, kRouteThreads, 0, stream>>>(topk_ids, S, k, E, nullptr, 1,
+                                                         expert_offsets, expert_counts,
+                                                         row_token, slot_of, rows_bound, status);
+    return cudaGetLastError();
+  }
   route_count_kernel<<<n_chunks, kRouteThreads, 0, stream>>>(topk_ids, S, E, chunk_counts,
                                                              row_token, rows_bound, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   route_assign_kernel<<<n_chunks, kRouteThreads, 0, stream>>>(
       topk_ids, S, k, E, chunk_counts, n_chunks, expert_offsets, expert_counts, row_token,
-      slot_of);
+      slot_of, rows_bound, status);
   return cudaGetLastError();
 }
 
