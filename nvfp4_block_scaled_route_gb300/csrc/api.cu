@@ -40,12 +40,13 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 2-D uint8 tensor [rows, row_bytes], box 128 x 128 bytes, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, int64_t row_bytes, int64_t rows) {
+bool make_map(CUtensorMap* map, const void* base, int64_t row_bytes, int64_t rows,
+              uint32_t box_rows = 128) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -330,11 +331,14 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   if (nsm <= 0) return NVMOE_ERR_CUDA;
   if (nsm > kMaxGrid) nsm = kMaxGrid;
 
-  CUtensorMap map_x, map_w1, map_h, map_w2;
+  AMaps map_x, map_h;
+  CUtensorMap map_w1, map_w2;
   const int64_t kt1 = ceil_div(H, kStageK), kt2 = ceil_div(I, kStageK);
-  if (!make_map(&map_x, xq, H / 2, rows) ||
+  if (!make_map(&map_x.full, xq, H / 2, rows) ||
+      !make_map(&map_x.small, xq, H / 2, rows, kSmallABoxRows) ||
       !make_tiled_map(&map_w1, w->w1, int64_t(E) * 2 * I / kTileRows * kt1) ||
-      !make_map(&map_h, b.hq, I / 2, rows) ||
+      !make_map(&map_h.full, b.hq, I / 2, rows) ||
+      !make_map(&map_h.small, b.hq, I / 2, rows, kSmallABoxRows) ||
       !make_tiled_map(&map_w2, w->w2, int64_t(E) * H / kTileRows * kt2))
     return NVMOE_ERR_CUDA;
 

@@ -164,13 +164,13 @@ struct WorkIter {
 // One grouped GEMM as the roles see it.
 struct Phase {
   const GemmArgs* a;
-  const CUtensorMap* map_a;
+  const AMaps* map_a;
   const CUtensorMap* map_b;
   const int* prefix;
   int total_tiles, k_blocks, k_stages, k_atoms;
 };
 
-__device__ __forceinline__ Phase make_phase(const GemmArgs& a, const CUtensorMap* ma,
+__device__ __forceinline__ Phase make_phase(const GemmArgs& a, const AMaps* ma,
                                             const CUtensorMap* mb, const int* prefix, int E) {
   Phase p;
   p.a = &a;
@@ -333,12 +333,17 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
   const uint64_t pol_a = policy_evict_last();
   const uint64_t pol_b = policy_evict_first();
   bool gate_open = gate == nullptr;
-  // activation loads waiting for the gate: (stage, a_row, ks)
+  // activation loads waiting for the gate: (stage, a_row, ks, small box)
   int def_stage[kStages], def_row[kStages], def_ks[kStages];
+  bool def_small[kStages];
   int n_def = 0;
-  auto issue_a = [&](int stage, int a_row, int ks) {
+  // An m-tile with at most kSmallABoxRows valid rows loads only those rows of
+  // A; the MMA still runs 128 rows, and the stale rows only produce
+  // accumulator rows that are never stored.
+  auto issue_a = [&](int stage, int a_row, int ks, bool small) {
     uint64_t* full = &bars->full[stage];
-    tma_load_2d(smem + kOffA + stage * kABytes, P.map_a, ks * kRowBytes, a_row, full, pol_a);
+    tma_load_2d(smem + kOffA + stage * kABytes, small ? &P.map_a->small : &P.map_a->full,
+                ks * kRowBytes, a_row, full, pol_a);
     const uint8_t* sfa = args.a_sf +
                          (static_cast<size_t>(a_row / 128) * P.k_atoms + ks * 4) * kSfAtomBytes;
     bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa, kSfaBytes, full, pol_a);
@@ -346,7 +351,7 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
   auto open_gate = [&]() -> bool {
     if (!wait_flag(gate, gate_target, args.status, abort)) return false;
     gate_open = true;
-    for (int i = 0; i < n_def; ++i) issue_a(def_stage[i], def_row[i], def_ks[i]);
+    for (int i = 0; i < n_def; ++i) issue_a(def_stage[i], def_row[i], def_ks[i], def_small[i]);
     n_def = 0;
     return true;
   };
@@ -355,6 +360,8 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
   while (ok && it.next(tile, s0, s1)) {
     const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
     const int a_row = tb.off[ti.e] + ti.mt * kBM;
+    const bool small_a = tb.cnt[ti.e] - ti.mt * kBM <= kSmallABoxRows;
+    const uint32_t tx = small_a ? kStageTx - (kBM - kSmallABoxRows) * kRowBytes : kStageTx;
     int b_row0, b_row1;
     if (args.mode == 1) {
       b_row0 = ti.e * args.N + ti.nt * 128;
@@ -379,7 +386,7 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
       }
       const int stage = pp.stage;
       uint64_t* full = &bars->full[stage];
-      mbar_arrive_expect_tx(full, kStageTx);
+      mbar_arrive_expect_tx(full, tx);
       tma_load_3d(smem + kOffB + stage * kBBytes, P.map_b, 0, 0, b_tile0 + ks, full, pol_b);
       tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, P.map_b, 0, 0, b_tile1 + ks,
                   full, pol_b);
@@ -388,11 +395,12 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
       bulk_load(smem + kOffSfb + stage * kSfbBytes + kSfaBytes, sfb1 + koff, kSfaBytes, full,
                 pol_b);
       if (gate_open) {
-        issue_a(stage, a_row, ks);
+        issue_a(stage, a_row, ks, small_a);
       } else {
         def_stage[n_def] = stage;
         def_row[n_def] = a_row;
         def_ks[n_def] = ks;
+        def_small[n_def] = small_a;
         ++n_def;
       }
       ++pp.issued;
@@ -671,7 +679,7 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 
 // ------------------------------------------------------------- kernels --
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+    const __grid_constant__ AMaps map_a, const __grid_constant__ CUtensorMap map_b,
     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
@@ -681,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   __shared__ int s_last, s_ok;
 
   load_tables(tb, args, args.n_tiles);
-  const uint32_t tmem = setup_cta(bars, &map_a, &map_b, nullptr, nullptr);
+  const uint32_t tmem = setup_cta(bars, &map_a.full, &map_b, &map_a.small, nullptr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars->abort;
   const Phase P = make_phase(args, &map_a, &map_b, tb.prefix1, args.E);
@@ -760,8 +768,8 @@ __device__ void requantise(const GemmArgs& a1, const FusedArgs& f, const Tables&
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
-    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w1,
-    const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w2,
+    const __grid_constant__ AMaps map_x, const __grid_constant__ CUtensorMap map_w1,
+    const __grid_constant__ AMaps map_h, const __grid_constant__ CUtensorMap map_w2,
     const GemmArgs a1, const GemmArgs a2, const FusedArgs f) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
@@ -771,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
   __shared__ int s_last, s_ok;
 
   load_tables(tb, a1, a2.n_tiles);
-  const uint32_t tmem = setup_cta(bars, &map_x, &map_w1, &map_h, &map_w2);
+  const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars->abort;
   const int E = a1.E;
@@ -821,7 +829,7 @@ bool g_fused_attr = false;
 
 int gemm_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_gemm(const GemmArgs& args, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
                         int grid, cudaStream_t stream) {
   if (!g_gemm_attr) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel,
@@ -834,8 +842,8 @@ cudaError_t launch_gemm(const GemmArgs& args, const CUtensorMap& map_a, const CU
   return cudaGetLastError();
 }
 
-cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const CUtensorMap& map_x,
-                             const CUtensorMap& map_w1, const CUtensorMap& map_h,
+cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps& map_x,
+                             const CUtensorMap& map_w1, const AMaps& map_h,
                              const CUtensorMap& map_w2, int* grid_bar, const int32_t* row_token,
                              uint8_t* hq, uint8_t* hsf, float* gs_h, int grid,
                              cudaStream_t stream) {

@@ -82,13 +82,21 @@ struct GemmArgs {
 };
 constexpr int kMaxGrid = 256;
 constexpr int kMaxSplitTiles = 4 * kMaxGrid;
-cudaError_t launch_gemm(const GemmArgs& args, const CUtensorMap& map_a, const CUtensorMap& map_b,
+// Activation (A operand) maps of one matrix: 128-row boxes, and 32-row boxes
+// used for m-tiles with at most 32 valid rows (decode), so that padding rows
+// are not fetched.
+struct AMaps {
+  CUtensorMap full;
+  CUtensorMap small;
+};
+constexpr int kSmallABoxRows = 32;
+cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
                         int grid, cudaStream_t stream);
 int gemm_smem_bytes();
 // L1 -> grid barrier -> requantise -> grid barrier -> L2 in one cooperative
 // launch (grid <= SM count, one CTA per SM).
-cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const CUtensorMap& map_x,
-                             const CUtensorMap& map_w1, const CUtensorMap& map_h,
+cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps& map_x,
+                             const CUtensorMap& map_w1, const AMaps& map_h,
                              const CUtensorMap& map_w2, int* grid_bar, const int32_t* row_token,
                              uint8_t* hq, uint8_t* hsf, float* gs_h, int grid,
                              cudaStream_t stream);
