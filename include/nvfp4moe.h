@@ -120,6 +120,34 @@ int moe_route_permute(const int32_t* topk_ids, int64_t T, int k, int E,
                       int32_t* row_token, int32_t* slot_of,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_route_permute_noalloc — the same routing permutation for callers that
+ * cannot hand the library a device workspace.  No counterpart in the source
+ * pages: it exists for callers that may not allocate device memory at all,
+ * e.g. a serving engine that reserves every byte of HBM up front for its own
+ * pools, or a plug-in host that owns all allocation, where a cudaMalloc
+ * (which also synchronises the device) is not permitted.
+ *
+ * Same arguments and results as moe_route_permute, without the workspace.
+ * The per-chunk histograms live in a fixed array inside the library
+ * (NVMOE_NOALLOC_ROUTE_WORDS 32-bit words, 256 KiB, held on every GPU that
+ * loads the library until the process exits); the call allocates nothing.
+ *   - Limit: ceil(T*k / 4096) * E <= NVMOE_NOALLOC_ROUTE_WORDS (for example
+ *     T*k up to 5.5 million slots with E = 48); larger inputs return
+ *     NVMOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array: calls whose kernels can overlap on the
+ *     GPU (different streams without ordering, or several host threads) race
+ *     and give wrong results.  Order them on one stream.
+ *   - An expert id outside [0, E) is dropped (slot_of = -1) but no status
+ *     word is written (there is no workspace to hold it).
+ */
+#define NVMOE_NOALLOC_ROUTE_WORDS (64 * 1024)
+int moe_route_permute_noalloc(const int32_t* topk_ids, int64_t T, int k, int E,
+                              int32_t* expert_offsets, int32_t* expert_counts,
+                              int32_t* row_token, int32_t* slot_of, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- step 2 --
  * nvfp4_quantize_act — dynamic NVFP4 quantisation of activations
  * ("NVFP4 MegaMoE Debug Log", Hypotheses §6 steps 1-5 and §5 packing; commit

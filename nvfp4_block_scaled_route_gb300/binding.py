@@ -57,6 +57,7 @@ SIGNATURES = {
     "moe_route_rows_bound": (_I64, [_I64, _I, _I]),
     "moe_route_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_route_permute": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_route_permute_noalloc": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "nvfp4_quantize_workspace_size": (_SZ, [_I64, _I64]),
     "nvfp4_quantize_act": (_I, [_P, _I, _I64, _I64, _P, _I, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_quantize_weights_workspace_size": (_SZ, [_I, _I, _I]),

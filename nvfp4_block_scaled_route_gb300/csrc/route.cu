@@ -172,3 +172,64 @@ cudaError_t launch_route(const int32_t* topk_ids, int64_t T, int k, int E,
 }
 
 }  // namespace nvmoe
+
+// ------------------------------------------------------------- no-alloc ----
+// Routing without a caller workspace: the per-chunk histograms go to a fixed
+// array in this library (every GPU that loads it holds the array until the
+// process exits).  Host code cannot use the array's name as a device address,
+// so the address is looked up once per device with cudaGetSymbolAddress.
+#include <mutex>
+
+#include "nvfp4moe.h"
+
+namespace {
+
+static __device__ __align__(256) int32_t g_noalloc_route_counts[NVMOE_NOALLOC_ROUTE_WORDS];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the array on the current device (looked up on first use).
+int noalloc_counts(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return NVMOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_route_counts) != cudaSuccess || p == nullptr)
+      return NVMOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return NVMOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_route_permute_noalloc(const int32_t* topk_ids, int64_t T, int k, int E,
+                                         int32_t* expert_offsets, int32_t* expert_counts,
+                                         int32_t* row_token, int32_t* slot_of,
+                                         cudaStream_t stream) {
+  using namespace nvmoe;
+  if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts) return NVMOE_ERR_INVALID_ARG;
+  if (T * k >= (int64_t(1) << 31)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (expert_offsets == nullptr || expert_counts == nullptr) return NVMOE_ERR_INVALID_ARG;
+  if (T > 0 && (topk_ids == nullptr || row_token == nullptr || slot_of == nullptr))
+    return NVMOE_ERR_INVALID_ARG;
+  const int64_t S = T * k;
+  const int64_t n_chunks = S > 0 ? ceil_div(S, kChunk) : 1;
+  if (n_chunks * E > NVMOE_NOALLOC_ROUTE_WORDS) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  int32_t* counts = nullptr;
+  const int st = noalloc_counts(&counts);
+  if (st != NVMOE_OK) return st;
+  // every word a launch reads is written by the same launch's counting pass
+  // (one chunk needs no histogram words at all), so nothing is cleared here
+  const int64_t S_pad = S + (S < E ? S : E) * (kTileRows - 1);
+  const int64_t rows = (S_pad + kTileRows - 1) / kTileRows * kTileRows;
+  const cudaError_t e = launch_route(topk_ids, T, k, E, expert_offsets, expert_counts, row_token,
+                                     rows, slot_of, counts, static_cast<int>(n_chunks), nullptr,
+                                     stream);
+  return e == cudaSuccess ? NVMOE_OK : NVMOE_ERR_CUDA;
+}
