@@ -238,18 +238,21 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "quant.cuh", "internal.h")
+
+
 def gemm_source_hash():
     h = hashlib.sha256()
-    for name in ("gemm.cu", "ptx.cuh"):
+    for name in GEMM_SOURCES:
         with open(os.path.join(ROOT, "nvfp4_block_scaled_route_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: str):
-    """dram bytes per L1 launch from the committed ncu summary, if it was
-    taken on the current GEMM source; else None."""
-    path = os.path.join(ROOT, "profiles", "l1_gemm_traffic.json")
+def profiled_traffic(kernel: str, config: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -410,7 +413,7 @@ def main():
                 "frac": achieved / peak, "peak_source": f"{peak_src} bf16 x {FP4_OVER_BF16} nominal fp4/bf16",
                 "kernel": "grouped_gemm_kernel (L1, mode 1)",
                 "algorithmic_flops_per_launch": l1_flops, "launch_ms": l1_ms}
-    roof["traffic"] = profiled_traffic(args.config)
+    roof["traffic"] = profiled_traffic(roof["kernel"].split()[0], args.config)
     step_bytes = l1_bytes + l2_bytes
 
     # ---- end to end from pinned host buffers through the public API ----
