@@ -255,6 +255,7 @@ typedef struct {
 #define NVMOE_PATH_AUTO 0
 #define NVMOE_PATH_SEPARATE 1
 #define NVMOE_PATH_FUSED 2
+#define NVMOE_PATH_LAYER 3     /* moe_nvfp4_layer_forward only */
 typedef struct {
   float* l1_out;
   float* h;
@@ -263,6 +264,7 @@ typedef struct {
   float* gs_h;
   cudaEvent_t stage_events[4];
   int path;
+  int32_t* slot_of;       /* moe_nvfp4_layer_forward: int32 [T*k] row of each slot */
 } nvmoe_taps;
 
 /* moe_nvfp4_forward — the expert FFN on grouped slots ("NVFP4 MegaMoE Debug
@@ -309,6 +311,32 @@ int moe_nvfp4_forward(const nvmoe_weights* weights, const uint8_t* xq,
 int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of,
                          const float* topk_w, int64_t T, int k, int64_t H,
                          void* y, int y_dtype, cudaStream_t stream);
+
+/* ----------------------------------------------------------- steps 1-7 --
+ * moe_nvfp4_layer_forward — the whole layer in one call: the four steps
+ * above on buffers carved from one workspace, with the same results.
+ *   x        [T, H] of x_dtype (NVMOE_BF16 or NVMOE_F32)
+ *   topk_ids int32 [T, k];  topk_w float [T, k]
+ *   y        [T, H] of y_dtype
+ * Small batches (bf16 x, T*k <= 128, T*H <= 65536, fewer than 4 tiles per SM
+ * in both GEMMs) run as ONE cooperative kernel: every CTA builds the routing
+ * tables and quantises the activation rows of its own tiles, so weight
+ * streaming starts at once; a single grid barrier separates L1 from the
+ * requantisation (the intermediate global scale needs every h); the top-k
+ * reduce of a (token, 256-column tile) is done by the CTA that writes its
+ * last slot row.  taps->path = NVMOE_PATH_LAYER forces that kernel
+ * (NVMOE_ERR_UNSUPPORTED_SHAPE when the batch is too large); SEPARATE / FUSED
+ * select the paths of moe_nvfp4_forward after separate routing and
+ * quantisation launches.  taps->slot_of, when given, receives the slot row
+ * of every (token, choice).
+ * Workspace: moe_nvfp4_layer_workspace_size bytes, zero-filled before first
+ * use; its status word (nvmoe_read_status) is the forward's.
+ */
+size_t moe_nvfp4_layer_workspace_size(int64_t T, int k, int E, int H, int I);
+int moe_nvfp4_layer_forward(const nvmoe_weights* weights, const void* x, int x_dtype,
+                            const int32_t* topk_ids, const float* topk_w, int64_t T, int k,
+                            void* y, int y_dtype, const nvmoe_taps* taps, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

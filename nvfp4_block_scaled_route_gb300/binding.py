@@ -39,10 +39,11 @@ class Weights(ctypes.Structure):
 class Taps(ctypes.Structure):
     _fields_ = [("l1_out", ctypes.c_void_p), ("h", ctypes.c_void_p), ("hq", ctypes.c_void_p),
                 ("hsf_mma", ctypes.c_void_p), ("gs_h", ctypes.c_void_p),
-                ("stage_events", ctypes.c_void_p * 4), ("path", ctypes.c_int)]
+                ("stage_events", ctypes.c_void_p * 4), ("path", ctypes.c_int),
+                ("slot_of", ctypes.c_void_p)]
 
 
-PATH_AUTO, PATH_SEPARATE, PATH_FUSED = 0, 1, 2
+PATH_AUTO, PATH_SEPARATE, PATH_FUSED, PATH_LAYER = 0, 1, 2, 3
 
 
 # name -> (restype, argtypes)
@@ -68,6 +69,9 @@ SIGNATURES = {
     "moe_nvfp4_forward": (_I, [ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _I64, _I, _P,
                                ctypes.POINTER(Taps), _P, _SZ, _P]),
     "moe_unpermute_reduce": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _I, _P]),
+    "moe_nvfp4_layer_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
+    "moe_nvfp4_layer_forward": (_I, [ctypes.POINTER(Weights), _P, _I, _P, _P, _I64, _I, _P, _I,
+                                     ctypes.POINTER(Taps), _P, _SZ, _P]),
 }
 
 
@@ -243,6 +247,24 @@ def forward_workspace_bytes(T: int, k: int, E: int, H: int, I: int) -> int:
     return int(lib().moe_nvfp4_workspace_size(T, k, E, H, I))
 
 
+def _taps(taps: Optional[dict]):
+    if not taps:
+        return None
+    t = Taps(_ptr(taps.get("l1_out")), _ptr(taps.get("h")), _ptr(taps.get("hq")),
+             _ptr(taps.get("hsf_mma")), _ptr(taps.get("gs_h")))
+    evs = taps.get("stage_events")
+    if evs is not None:
+        # torch events are created on first record; their handles are plain
+        # CUDA event handles
+        for i, ev in enumerate(evs):
+            if ev.cuda_event == 0:
+                ev.record()
+            t.stage_events[i] = ev.cuda_event
+    t.path = int(taps.get("path", PATH_AUTO))
+    t.slot_of = _ptr(taps.get("slot_of"))
+    return t
+
+
 def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Tensor,
                   gs_x: torch.Tensor, route: Route, slot_out: Optional[torch.Tensor] = None,
                   taps: Optional[dict] = None, ws: Optional[torch.Tensor] = None, stream=None):
@@ -252,19 +274,7 @@ def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Ten
     if ws is None:
         ws = _workspace(forward_workspace_bytes(route.T, route.k, weights.E, weights.H,
                                                 weights.I), dev)
-    t = None
-    if taps:
-        t = Taps(_ptr(taps.get("l1_out")), _ptr(taps.get("h")), _ptr(taps.get("hq")),
-                 _ptr(taps.get("hsf_mma")), _ptr(taps.get("gs_h")))
-        evs = taps.get("stage_events")
-        if evs is not None:
-            # torch events are created on first record; their handles are
-            # plain CUDA event handles
-            for i, ev in enumerate(evs):
-                if ev.cuda_event == 0:
-                    ev.record()
-                t.stage_events[i] = ev.cuda_event
-        t.path = int(taps.get("path", PATH_AUTO))
+    t = _taps(taps)
     wst = weights.struct()
     _check("moe_nvfp4_forward", lib().moe_nvfp4_forward(
         ctypes.byref(wst), _ptr(xq), _ptr(xsf_mma), _ptr(gs_x), _ptr(route.expert_offsets),
@@ -333,3 +343,34 @@ class MoELayer:
             if s:
                 return s
         return 0
+
+
+class FusedLayer:
+    """The whole layer through one call (moe_nvfp4_layer_forward) on one
+    preallocated workspace.  Small batches run as a single cooperative
+    kernel; larger ones as route, quantise, forward and reduce launches."""
+
+    def __init__(self, weights: PreparedWeights, T: int, k: int, device="cuda",
+                 out_dtype=torch.bfloat16):
+        self.w = weights
+        self.T, self.k = T, k
+        dev = torch.device(device)
+        self.rows = rows_bound(T, k, weights.E)
+        self.ws = _workspace(lib().moe_nvfp4_layer_workspace_size(T, k, weights.E, weights.H,
+                                                                   weights.I), dev)
+        self.y = torch.empty((T, weights.H), dtype=out_dtype, device=dev)
+        self._w = weights.struct()
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
+                taps: Optional[dict] = None, stream=None) -> torch.Tensor:
+        xcode = {torch.bfloat16: BF16, torch.float32: F32}[x.dtype]
+        ycode = {torch.bfloat16: BF16, torch.float32: F32}[self.y.dtype]
+        t = _taps(taps)
+        _check("moe_nvfp4_layer_forward", lib().moe_nvfp4_layer_forward(
+            ctypes.byref(self._w), _ptr(x), xcode, _ptr(topk_ids), _ptr(topk_w), self.T, self.k,
+            _ptr(self.y), ycode, ctypes.byref(t) if t is not None else None, _ptr(self.ws),
+            self.ws.numel(), _stream(stream)))
+        return self.y
+
+    def status(self) -> int:
+        return read_status(self.ws)

@@ -289,11 +289,28 @@ size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I) {
   return forward_layout(T, k, E, I, nullptr, &b);
 }
 
+// Steps 3-6 (and, with `layer`, the whole layer in one launch).
+static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
+                        const float* gs_x, const int32_t* expert_offsets,
+                        const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
+                        float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
+                        cudaStream_t stream, LayerLaunch* layer);
+
 int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
                       const float* gs_x, const int32_t* expert_offsets,
                       const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
                       float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
                       cudaStream_t stream) {
+  if (taps != nullptr && taps->path == NVMOE_PATH_LAYER) return NVMOE_ERR_INVALID_ARG;
+  return forward_impl(w, xq, xsf_mma, gs_x, expert_offsets, expert_counts, row_token, T, k,
+                      slot_out, taps, ws, ws_bytes, stream, nullptr);
+}
+
+static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
+                        const float* gs_x, const int32_t* expert_offsets,
+                        const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
+                        float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
+                        cudaStream_t stream, LayerLaunch* layer) {
   if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
   const int E = w->E, H = w->H, I = w->I;
   if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;
@@ -309,7 +326,8 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
   if (ws_bytes < moe_nvfp4_workspace_size(T, k, E, H, I)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
   int path = NVMOE_PATH_AUTO;
   if (taps != nullptr) path = taps->path;
-  if (path != NVMOE_PATH_AUTO && path != NVMOE_PATH_SEPARATE && path != NVMOE_PATH_FUSED)
+  if (path != NVMOE_PATH_AUTO && path != NVMOE_PATH_SEPARATE && path != NVMOE_PATH_FUSED &&
+      path != NVMOE_PATH_LAYER)
     return NVMOE_ERR_INVALID_ARG;
   if (T == 0) return NVMOE_OK;
   FwdBuffers b;
@@ -394,6 +412,18 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
                      (path == NVMOE_PATH_AUTO && tiles1 < 4 * int64_t(nsm) && tiles2 < 4 * int64_t(nsm));
   const bool timed = ev[0] && ev[1] && ev[2] && ev[3];
   if (timed && cudaEventRecord(ev[0], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (layer != nullptr) {
+    layer->hq = b.hq;
+    layer->hsf = b.hsf;
+    layer->gs_h = b.gs_h;
+    const int g = grid_for(tiles1 > tiles2 ? tiles1 : tiles2);
+    cudaError_t e = counted(launch_layer(a1, a2, map_x, map_w1, map_h, map_w2, *layer, g, stream), 1);
+    if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+    if (timed)
+      for (int i = 1; i < 4; ++i)
+        if (cudaEventRecord(ev[i], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+    return NVMOE_OK;
+  }
   if (fused) {
     const int g = grid_for(tiles1 > tiles2 ? tiles1 : tiles2);
     cudaError_t e = counted(launch_fused_ffn(a1, a2, map_x, map_w1, map_h, map_w2, b.grid_bar,
@@ -433,6 +463,120 @@ int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of, const fl
     return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(slot_out) || !aligned16(y)) return NVMOE_ERR_MISALIGNED;
   return status_of(counted(launch_reduce(slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream), 1));
+}
+
+// ------------------------------------------------------------- layer ----
+struct LayerBuffers {
+  uint8_t* fwd_ws;        // first: its status word is the layer workspace's
+  size_t fwd_ws_bytes;
+  int32_t* offsets;
+  int32_t* counts;
+  int32_t* row_token;
+  int32_t* slot_of;
+  uint8_t* route_ws;
+  size_t route_ws_bytes;
+  uint8_t* xq;
+  uint8_t* xsf;
+  float* gs_x;
+  uint8_t* quant_ws;
+  size_t quant_ws_bytes;
+  float* slot_out;
+  int* grid_bar;
+  int* ycnt;
+};
+
+static size_t layer_layout(int64_t T, int k, int E, int H, int I, uint8_t* base,
+                           LayerBuffers* b) {
+  Carve c{base};
+  const int64_t rows = rows_bound(T, k, E);
+  b->fwd_ws_bytes = moe_nvfp4_workspace_size(T, k, E, H, I);
+  b->fwd_ws = c.take<uint8_t>(b->fwd_ws_bytes);
+  b->offsets = c.take<int32_t>((E + 1) * sizeof(int32_t));
+  b->counts = c.take<int32_t>(E * sizeof(int32_t));
+  b->row_token = c.take<int32_t>((rows > 0 ? rows : 1) * sizeof(int32_t));
+  b->slot_of = c.take<int32_t>((T * k > 0 ? T * k : 1) * sizeof(int32_t));
+  b->route_ws_bytes = moe_route_workspace_size(T, k, E);
+  b->route_ws = c.take<uint8_t>(b->route_ws_bytes);
+  b->xq = c.take<uint8_t>(static_cast<size_t>(rows) * (H / 2));
+  b->xsf = c.take<uint8_t>(sf_mma_bytes(rows, H));
+  b->gs_x = c.take<float>(sizeof(float));
+  b->quant_ws_bytes = nvfp4_quantize_workspace_size(T, H);
+  b->quant_ws = c.take<uint8_t>(b->quant_ws_bytes);
+  b->slot_out = c.take<float>(static_cast<size_t>(rows) * H * sizeof(float));
+  b->grid_bar = c.take<int>(4 * sizeof(int));
+  b->ycnt = c.take<int>(static_cast<size_t>(T > 0 ? T : 1) * (H / 256 + 1) * sizeof(int));
+  return c.off;
+}
+
+size_t moe_nvfp4_layer_workspace_size(int64_t T, int k, int E, int H, int I) {
+  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return 0;
+  LayerBuffers b;
+  return layer_layout(T, k, E, H, I, nullptr, &b);
+}
+
+int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
+                            const int32_t* topk_ids, const float* topk_w, int64_t T, int k,
+                            void* y, int y_dtype, const nvmoe_taps* taps, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  const int E = w->E, H = w->H, I = w->I;
+  if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;
+  if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (y_dtype != NVMOE_BF16 && y_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws == nullptr) return NVMOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_ids == nullptr || topk_w == nullptr || y == nullptr))
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < moe_nvfp4_layer_workspace_size(T, k, E, H, I))
+    return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  const int path = taps != nullptr ? taps->path : NVMOE_PATH_AUTO;
+  if (T == 0) return NVMOE_OK;
+  LayerBuffers b;
+  layer_layout(T, k, E, H, I, static_cast<uint8_t*>(ws), &b);
+  int32_t* slot_of = (taps != nullptr && taps->slot_of != nullptr) ? taps->slot_of : b.slot_of;
+  const int64_t S = T * k;
+  const int64_t rows = rows_bound(T, k, E);
+
+  int nsm = sm_count();
+  if (nsm <= 0) return NVMOE_ERR_CUDA;
+  const int64_t mt_bound = S / kTileRows + (S < E ? S : E);
+  const bool small = x_dtype == NVMOE_BF16 && S <= kLayerMaxSlots &&
+                     T * H <= kQuantSmallElems && mt_bound * (I / 128) < 4 * int64_t(nsm) &&
+                     mt_bound * (H / 256) < 4 * int64_t(nsm);
+  if (path == NVMOE_PATH_LAYER && !small) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (path == NVMOE_PATH_LAYER || (path == NVMOE_PATH_AUTO && small)) {
+    LayerLaunch l{};
+    l.x = x;
+    l.topk_ids = topk_ids;
+    l.topk_w = topk_w;
+    l.T = static_cast<int>(T);
+    l.k = k;
+    l.rows = rows;
+    l.xq = b.xq;
+    l.xsf = b.xsf;
+    l.gs_x = b.gs_x;
+    l.expert_offsets = b.offsets;
+    l.expert_counts = b.counts;
+    l.row_token = b.row_token;
+    l.slot_of = slot_of;
+    l.grid_bar = b.grid_bar;
+    l.ycnt = b.ycnt;
+    l.y = y;
+    l.y_dtype = y_dtype;
+    return forward_impl(w, b.xq, b.xsf, b.gs_x, b.offsets, b.counts, b.row_token, T, k,
+                        b.slot_out, taps, b.fwd_ws, b.fwd_ws_bytes, stream, &l);
+  }
+  int st = moe_route_permute(topk_ids, T, k, E, b.offsets, b.counts, b.row_token, slot_of,
+                             b.route_ws, b.route_ws_bytes, stream);
+  if (st != NVMOE_OK) return st;
+  st = nvfp4_quantize_act(x, x_dtype, T, H, slot_of, k, rows, b.xq, nullptr, b.xsf, b.gs_x,
+                          b.quant_ws, b.quant_ws_bytes, stream);
+  if (st != NVMOE_OK) return st;
+  st = forward_impl(w, b.xq, b.xsf, b.gs_x, b.offsets, b.counts, b.row_token, T, k, b.slot_out,
+                    taps, b.fwd_ws, b.fwd_ws_bytes, stream, nullptr);
+  if (st != NVMOE_OK) return st;
+  return moe_unpermute_reduce(b.slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream);
 }
 
 }  // extern "C"

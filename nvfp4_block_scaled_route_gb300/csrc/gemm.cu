@@ -32,6 +32,8 @@
 //   SFA 4 atoms (2 KB), SFB 2 x 4 atoms (4 KB) of 512-byte scale atoms.
 // TMEM (512 columns): accumulator in columns [0, 256); scale slots of
 // stage s at 256 + 48 s: SFA 4 columns per 64-element k-block, SFB 8.
+#include <cuda_bf16.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -319,14 +321,22 @@ __device__ bool grid_barrier(int* bar, int generation, int* status, volatile int
   return wait_flag(&bar[1], generation, status, abort);
 }
 
+// What the activation (A) loads of a phase wait for: a global generation
+// flag (grid barrier) or a shared-memory mbarrier completed by this CTA's
+// epilogue warps once they have written the rows the CTA needs.
+struct Gate {
+  const int* flag;
+  int target;
+  uint64_t* bar;
+};
+
 // ------------------------------------------------------------ producer --
 // Issues the loads of every stage of this CTA's items.  When `gate` is
-// given, the A-operand (activation) loads wait until *gate >= gate_target:
-// the weight (B) loads of the first stages go out first and the activation
-// loads follow once the gate opens.
+// given, the A-operand (activation) loads wait until the gate opens: the
+// weight (B) loads of the first stages go out first and the activation
+// loads follow.
 __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* bars,
-                             uint8_t* smem, Pipe& pp, volatile int* abort, const int* gate,
-                             int gate_target) {
+                             uint8_t* smem, Pipe& pp, volatile int* abort, const Gate* gate) {
   const GemmArgs& args = *P.a;
   WorkIter it;
   it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
@@ -349,7 +359,12 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
     bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa, kSfaBytes, full, pol_a);
   };
   auto open_gate = [&]() -> bool {
-    if (!wait_flag(gate, gate_target, args.status, abort)) return false;
+    if (gate->bar != nullptr) {
+      if (!mbar_wait(gate->bar, 0, args.status, abort)) return false;
+      fence_proxy_async_global();
+    } else if (!wait_flag(gate->flag, gate->target, args.status, abort)) {
+      return false;
+    }
     gate_open = true;
     for (int i = 0; i < n_def; ++i) issue_a(def_stage[i], def_row[i], def_ks[i], def_small[i]);
     n_def = 0;
@@ -476,11 +491,87 @@ __device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t 
 }
 
 // ------------------------------------------------------------ epilogue --
+// Top-k weighted reduce done inside the layer kernel: when the last of a
+// token's k slot rows of one 256-column tile of slot_out is written, the
+// CTA that wrote it sums the k rows (ascending j, fp32, the same arithmetic
+// as unpermute_reduce_kernel) into y.
+struct YReduce {
+  int* counts;              // [T][n_tiles], zero between calls
+  const float* topk_w;      // [T, k]
+  const int* slot_row;      // [T*k] (shared memory)
+  const int* dense_token;   // dense slot -> token (shared memory)
+  void* y;
+  int y_dtype;              // 0 bf16, 1 fp32
+  int k;
+  int n_tiles;
+  int* s_list;              // [kBM] shared memory
+  int* s_n;                 // shared memory
+};
+
+__device__ void y_after_tile(const YReduce& yr, const TileInfo& ti, const Tables& tb,
+                             const GemmArgs& args) {
+  const int etid = threadIdx.x - 64;
+  const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
+  const int d0 = tb.dense[ti.e] + ti.mt * kBM;
+  const int H = args.N;
+  __threadfence();                       // this tile's slot_out rows, device-wide
+  if (etid == 0) *yr.s_n = 0;
+  epi_bar();
+  for (int r = etid; r < n_valid; r += 128) {
+    const int t = yr.dense_token[d0 + r];
+    int* c = &yr.counts[t * yr.n_tiles + ti.nt];
+    if (atomicAdd(c, 1) == yr.k - 1) {
+      *c = 0;
+      yr.s_list[atomicAdd(yr.s_n, 1)] = t;
+    }
+  }
+  epi_bar();
+  const int n = *yr.s_n;
+  if (n > 0) __threadfence();
+  for (int wi = etid; wi < n * (kBN / 4); wi += 128) {
+    const int t = yr.s_list[wi / (kBN / 4)];
+    const int col = ti.nt * kBN + (wi % (kBN / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < yr.k; j0 += 8) {
+      float4 v[8];
+      float wj[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < yr.k) {
+          const int s = yr.slot_row[t * yr.k + j0 + j];
+          v[j] = __ldcg(reinterpret_cast<const float4*>(args.out + static_cast<int64_t>(s) * H + col));
+          wj[j] = __ldg(yr.topk_w + t * yr.k + j0 + j);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < yr.k) {
+          acc.x = __fmaf_rn(wj[j], v[j].x, acc.x);
+          acc.y = __fmaf_rn(wj[j], v[j].y, acc.y);
+          acc.z = __fmaf_rn(wj[j], v[j].z, acc.z);
+          acc.w = __fmaf_rn(wj[j], v[j].w, acc.w);
+        }
+      }
+    }
+    if (yr.y_dtype == 0) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 o;
+      o.x = *reinterpret_cast<uint32_t*>(&lo);
+      o.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(yr.y) + static_cast<int64_t>(t) * H + col) = o;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(yr.y) + static_cast<int64_t>(t) * H + col) = acc;
+    }
+  }
+  epi_bar();
+}
+
 // Four warps (128 threads, one accumulator row each).  Returns false when
 // a wait gave up; the decision is shared so all four warps leave together.
 __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* bars,
                              uint32_t tmem, Pipe& pp, volatile int* abort, float& amax,
-                             int* s_ok, int* s_last) {
+                             int* s_ok, int* s_last, const YReduce* yr = nullptr) {
   const GemmArgs& args = *P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                      // TMEM lane quarter
@@ -522,6 +613,7 @@ __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->acc_empty);
+      if (yr != nullptr) y_after_tile(*yr, ti, tb, args);
     } else {
       // a piece of a split tile: park the raw accumulator in the workspace
       float* mine = args.partials +
@@ -585,6 +677,7 @@ __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* 
           else
             epi_l2_4(a, alpha, row0 + r, col0 + g4 * 4, args);
         }
+        if (yr != nullptr) y_after_tile(*yr, ti, tb, args);
       }
     }
     pp.acc_phase ^= 1u;
@@ -696,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   Pipe pp;
   if (warp == 0) {
     if (lane == 0) {
-      run_producer(P, args.E, tb, bars, smem, pp, abort, nullptr, 0);
+      run_producer(P, args.E, tb, bars, smem, pp, abort, nullptr);
       drain_producer(bars, pp, args.status);
     }
   } else if (warp == 1) {
@@ -788,8 +881,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
   Pipe pp;
   if (warp == 0) {
     if (lane == 0) {
-      if (run_producer(P1, E, tb, bars, smem, pp, abort, nullptr, 0))
-        run_producer(P2, E, tb, bars, smem, pp, abort, &f.grid_bar[1], 2);
+      const Gate g2{&f.grid_bar[1], 2, nullptr};
+      if (run_producer(P1, E, tb, bars, smem, pp, abort, nullptr))
+        run_producer(P2, E, tb, bars, smem, pp, abort, &g2);
       drain_producer(bars, pp, a1.status);
     }
   } else if (warp == 1) {
@@ -822,10 +916,323 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
   teardown_cta(bars, tmem);
 }
 
+// ------------------------------------------------------- layer kernel ----
+// The whole forward of a small batch in one cooperative launch: routing,
+// activation quantisation, L1, requantisation, L2 and the weighted reduce.
+//  * every CTA builds the routing tables itself from topk_ids (no barrier);
+//  * every CTA computes gs_x over all of x and quantises the activation rows
+//    of its own L1 m-tiles (several CTAs may write the same rows, with the
+//    same bytes), so its weight loads start at once and its activation loads
+//    only wait for its own epilogue warps;
+//  * one grid barrier after L1 (the intermediate global scale needs every h);
+//    then every CTA requantises the rows of its own L2 m-tiles;
+//  * the top-k reduce of a (token, 256-column tile) is done by the CTA that
+//    writes the last of the token's k slot rows of that tile.
+struct LayerArgs {
+  const __nv_bfloat16* x;     // [T, H]
+  const int32_t* topk_ids;    // [T, k]
+  const float* topk_w;        // [T, k]
+  int T, k;
+  int64_t rows;               // slot rows (moe_route_rows_bound)
+  uint8_t* xq;                // [rows, H/2]
+  uint8_t* xsf;               // staged scales of xq
+  float* gs_x;                // [1]
+  int32_t* expert_offsets;    // [E+1]   (written by CTA 0)
+  int32_t* expert_counts;     // [E]
+  int32_t* row_token;         // [rows]
+  int32_t* slot_of;           // [T*k]
+  int* grid_bar;              // [3] arrivals, generation, exits; zero between calls
+  int* ycnt;                  // [T * H/256], zero between calls
+  uint8_t* hq;
+  uint8_t* hsf;
+  float* gs_h;
+  void* y;
+  int y_dtype;
+};
+
+
+// Quantise, with scale gs, the valid rows of every m-tile this CTA works on
+// in phase P (epilogue warps).  Rows come from `src` (bf16 tokens through
+// dense_token, or fp32 slot rows), go to q / staged sf of the slot layout.
+template <bool kFromTokens>
+__device__ void quantise_own_rows(const Phase& P, const Tables& tb, int E, const void* src,
+                                  int cols, const int* dense_token, uint8_t* q, uint8_t* sf,
+                                  float gs) {
+  const int bpr = cols >> 4;
+  const int k_atoms = (cols + kStageK - 1) / kStageK * 4;
+  const float denom = __fmul_rn(6.0f, gs);
+  const int lane = threadIdx.x & 31;
+  const int ew = (threadIdx.x >> 5) - 2;
+  WorkIter it;
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  int seen_e[4], seen_mt[4], n_seen = 0;
+  int tile, s0, s1;
+  while (it.next(tile, s0, s1)) {
+    const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
+    bool dup = false;
+    for (int i = 0; i < n_seen; ++i) dup |= seen_e[i] == ti.e && seen_mt[i] == ti.mt;
+    if (dup) continue;
+    if (n_seen < 4) {
+      seen_e[n_seen] = ti.e;
+      seen_mt[n_seen] = ti.mt;
+      ++n_seen;
+    }
+    const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
+    const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
+    const int d0 = tb.dense[ti.e] + ti.mt * kBM;
+    const int total = n_valid * bpr;
+    for (int base = ew * 32; base < total; base += 128) {      // warp-uniform
+      const int i = base + lane;
+      const bool active = i < total;
+      const int r = active ? i / bpr : 0;
+      const int g = active ? i - r * bpr : 0;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      if (active) {
+        if (kFromTokens) {
+          const int t = dense_token[d0 + r];
+          const uint4* p = reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(src) + static_cast<int64_t>(t) * cols + g * 16);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint4 u = __ldg(p + c);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              v[8 * c + 2 * m] = __uint_as_float(w4[m] << 16);
+              v[8 * c + 2 * m + 1] = __uint_as_float(w4[m] & 0xFFFF0000u);
+            }
+          }
+        } else {
+          const float4* p = reinterpret_cast<const float4*>(
+              static_cast<const float*>(src) + (row0 + r) * cols + g * 16);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 f = __ldcg(p + c);
+            v[4 * c] = f.x; v[4 * c + 1] = f.y; v[4 * c + 2] = f.z; v[4 * c + 3] = f.w;
+          }
+        }
+      }
+      uint32_t packed[2];
+      const uint32_t s = quant_block16(v, gs, denom, packed);
+      const uint32_t sa = __shfl_down_sync(0xFFFFFFFFu, s, 1);
+      const uint32_t sb = __shfl_down_sync(0xFFFFFFFFu, s, 2);
+      const uint32_t sc = __shfl_down_sync(0xFFFFFFFFu, s, 3);
+      if (!active) continue;
+      *reinterpret_cast<uint2*>(q + (row0 + r) * (cols >> 1) + g * 8) =
+          make_uint2(packed[0], packed[1]);
+      if ((g & 3) == 0)
+        *reinterpret_cast<uint32_t*>(sf + staged_offset(row0 + r, g, k_atoms)) =
+            s | (sa << 8) | (sb << 16) | (sc << 24);
+    }
+  }
+  // the producer's TMA reads of these rows come after this (async proxy)
+  fence_proxy_async_global();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) layer_kernel(
+    const __grid_constant__ AMaps map_x, const __grid_constant__ CUtensorMap map_w1,
+    const __grid_constant__ AMaps map_h, const __grid_constant__ CUtensorMap map_w2,
+    const GemmArgs a1, const GemmArgs a2, const LayerArgs L) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+  __shared__ Tables tb;
+  __shared__ float s_amax[4];
+  __shared__ int s_last, s_ok, s_n;
+  __shared__ int s_row[kLayerMaxSlots];       // slot row of flat index t*k+j
+  __shared__ int s_tok[kLayerMaxSlots];       // token of dense slot
+  __shared__ int s_scratch[kMaxExperts];      // running counts, then the reduce list
+  __shared__ float s_gs;
+  __shared__ __align__(8) uint64_t s_gate[2];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a1.E, k = L.k, S = L.T * L.k;
+  const int H = a1.K, I = a1.I;
+
+  // ---- routing tables, in every CTA ----
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    tb.cnt[e] = 0;
+    s_scratch[e] = 0;
+  }
+  if (threadIdx.x == 0) s_amax[0] = 0.0f;
+  __syncthreads();
+  for (int i = threadIdx.x; i < S; i += blockDim.x) {
+    const int e = L.topk_ids[i];
+    if (e >= 0 && e < E)
+      atomicAdd(&tb.cnt[e], 1);
+    else if (blockIdx.x == 0)
+      record_status(a1.status, kErrBadIndex);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0, p1 = 0, p2 = 0, d = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = tb.cnt[e];
+      tb.off[e] = off;
+      tb.mtiles[e] = (c + kBM - 1) / kBM;
+      tb.prefix1[e] = p1;
+      tb.prefix2[e] = p2;
+      tb.dense[e] = d;
+      off += tb.mtiles[e] * kBM;
+      p1 += tb.mtiles[e] * a1.n_tiles;
+      p2 += tb.mtiles[e] * a2.n_tiles;
+      d += c;
+    }
+    tb.prefix1[E] = p1;
+    tb.prefix2[E] = p2;
+    tb.dense[E] = d;
+    if (blockIdx.x == 0) L.expert_offsets[E] = off;
+    mbar_init(&s_gate[0], 1);
+    mbar_init(&s_gate[1], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // stable rank inside each expert: one warp, 32 flat indices per round
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < S; base += 32) {
+      const int i = base + lane;
+      int e = i < S ? L.topk_ids[i] : -1;
+      if (e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      const int rank = __popc(peers & lt);
+      const int before = e >= 0 ? s_scratch[e] : 0;
+      __syncwarp();
+      if (e >= 0 && (peers >> lane) == 1u) s_scratch[e] = before + rank + 1;
+      __syncwarp();
+      if (i < S) {
+        s_row[i] = e >= 0 ? tb.off[e] + before + rank : -1;
+        if (e >= 0) s_tok[tb.dense[e] + before + rank] = i / k;
+      }
+    }
+  }
+  // ---- gs_x = amax(x) / 2688, in every CTA ----
+  {
+    const int64_t n_vec = static_cast<int64_t>(L.T) * H / 8;
+    float m = 0.0f;
+    for (int64_t i = threadIdx.x; i < n_vec; i += blockDim.x) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(L.x) + i);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[j] << 16)),
+                           fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+    }
+    m = warp_max(m);
+    // |x| >= 0, so the float bits order like the values
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(&s_amax[0]), __float_as_int(m));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_gs = global_scale_from(s_amax[0]);
+      if (blockIdx.x == 0) *L.gs_x = s_gs;
+    }
+  }
+  __syncthreads();
+  // ---- routing outputs for the caller (CTA 0) ----
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      L.expert_offsets[e] = tb.off[e];
+      L.expert_counts[e] = tb.cnt[e];
+    }
+    for (int64_t r = threadIdx.x; r < L.rows; r += blockDim.x) L.row_token[r] = -1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+      L.slot_of[i] = s_row[i];
+      if (s_row[i] >= 0) L.row_token[s_row[i]] = i / k;
+    }
+  }
+
+  const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2);
+  volatile int* abort = &bars->abort;
+  const Phase P1 = make_phase(a1, &map_x, &map_w1, tb.prefix1, E);
+  const Phase P2 = make_phase(a2, &map_h, &map_w2, tb.prefix2, E);
+  Pipe pp;
+  if (warp == 0) {
+    if (lane == 0) {
+      const Gate g1{nullptr, 0, &s_gate[0]};
+      const Gate g2{nullptr, 0, &s_gate[1]};
+      if (run_producer(P1, E, tb, bars, smem, pp, abort, &g1))
+        run_producer(P2, E, tb, bars, smem, pp, abort, &g2);
+      drain_producer(bars, pp, a1.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (run_mma(P1, bars, smem, tmem, pp, abort)) run_mma(P2, bars, smem, tmem, pp, abort);
+      mma_drain(bars, a1.status);
+    }
+  } else {
+    const bool lead = warp == 2 && lane == 0;
+    quantise_own_rows<true>(P1, tb, E, L.x, H, s_tok, L.xq, L.xsf, s_gs);
+    epi_bar();
+    if (lead) mbar_arrive(&s_gate[0]);
+    float amax = 0.0f;
+    bool ok = run_epilogue(P1, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    publish_amax(amax, s_amax, a1.amax_partial);
+    // the one grid barrier: every h row and every per-CTA amax is written
+    if (lead) s_ok = ok && grid_barrier(L.grid_bar, 1, a1.status, abort) ? 1 : 0;
+    epi_bar();
+    ok = s_ok != 0;
+    if (ok) {
+      const float gs = global_scale_from(reduce_partials(a1.amax_partial, gridDim.x));
+      if (blockIdx.x == 0 && lead) *L.gs_h = gs;
+      quantise_own_rows<false>(P2, tb, E, a1.out, I, nullptr, L.hq, L.hsf, gs);
+      epi_bar();
+      if (lead) mbar_arrive(&s_gate[1]);
+      YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
+                 s_scratch, &s_n};
+      run_epilogue(P2, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
+    } else if (lead) {
+      // let the producer's bounded gate wait end instead of timing out twice
+      mbar_arrive(&s_gate[1]);
+    }
+  }
+  teardown_cta(bars, tmem);
+  // last CTA out clears the barrier words for the next call
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&L.grid_bar[2], 1) == static_cast<int>(gridDim.x) - 1) {
+      L.grid_bar[0] = 0;
+      L.grid_bar[1] = 0;
+      L.grid_bar[2] = 0;
+      __threadfence();
+    }
+  }
+}
+
 bool g_gemm_attr = false;
 bool g_fused_attr = false;
+bool g_layer_attr = false;
 
 }  // namespace
+
+cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& map_x,
+                         const CUtensorMap& map_w1, const AMaps& map_h,
+                         const CUtensorMap& map_w2, const LayerLaunch& l, int grid,
+                         cudaStream_t stream) {
+  if (!g_layer_attr) {
+    cudaError_t err = cudaFuncSetAttribute(layer_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+    if (err != cudaSuccess) return err;
+    g_layer_attr = true;
+  }
+  LayerArgs L{static_cast<const __nv_bfloat16*>(l.x), l.topk_ids, l.topk_w, l.T, l.k, l.rows,
+              l.xq, l.xsf, l.gs_x, l.expert_offsets, l.expert_counts, l.row_token, l.slot_of,
+              l.grid_bar, l.ycnt, l.hq, l.hsf, l.gs_h, l.y, l.y_dtype};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, layer_kernel, map_x, map_w1, map_h, map_w2, a1, a2, L);
+}
 
 int gemm_smem_bytes() { return kSmemBytes; }
 

@@ -95,6 +95,34 @@ cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensor
 int gemm_smem_bytes();
 // L1 -> grid barrier -> requantise -> grid barrier -> L2 in one cooperative
 // launch (grid <= SM count, one CTA per SM).
+// The whole forward of a small batch (routing .. reduce) in one cooperative
+// launch; limits: T*k <= kLayerMaxSlots, T*H <= kQuantSmallElems, bf16 x.
+constexpr int kLayerMaxSlots = 128;
+struct LayerLaunch {
+  const void* x;              // bf16 [T, H]
+  const int32_t* topk_ids;
+  const float* topk_w;
+  int T, k;
+  int64_t rows;
+  uint8_t* xq;
+  uint8_t* xsf;
+  float* gs_x;
+  int32_t* expert_offsets;
+  int32_t* expert_counts;
+  int32_t* row_token;
+  int32_t* slot_of;
+  int* grid_bar;              // [3], zero between calls
+  int* ycnt;                  // [T * H/256], zero between calls
+  uint8_t* hq;
+  uint8_t* hsf;
+  float* gs_h;
+  void* y;
+  int y_dtype;
+};
+cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& map_x,
+                         const CUtensorMap& map_w1, const AMaps& map_h,
+                         const CUtensorMap& map_w2, const LayerLaunch& l, int grid,
+                         cudaStream_t stream);
 cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps& map_x,
                              const CUtensorMap& map_w1, const AMaps& map_h,
                              const CUtensorMap& map_w2, int* grid_bar, const int32_t* row_token,

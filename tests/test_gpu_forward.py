@@ -229,3 +229,91 @@ def test_forward_decode_full_size(nb):
     assert 2.0 < l1_amax < 40.0
     print(f"decode1: flips {flips}, l1 amax {l1_amax:.3f}, h amax {np.abs(ref['h']).max():.3f}, "
           f"out2 amax {np.abs(ref['out2']).max():.3f}, y amax {np.abs(ref['y64']).max():.3f}")
+
+
+def run_gpu_layer(nb, cfg, x, ids, w, W1_dev, W2_dev, out_dtype=torch.float32, path=3):
+    """The whole layer through moe_nvfp4_layer_forward (one call)."""
+    q1, s1, g1 = nb.quantize_weights(W1_dev)
+    q2, s2, g2 = nb.quantize_weights(W2_dev)
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    layer = nb.FusedLayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=out_dtype)
+    rows = layer.rows
+    taps = dict(l1_out=torch.zeros((rows, 2 * cfg.I), dtype=torch.float32, device=DEV),
+                h=torch.zeros((rows, cfg.I), dtype=torch.float32, device=DEV),
+                hq=torch.zeros((rows, cfg.I // 2), dtype=torch.uint8, device=DEV),
+                hsf_mma=torch.zeros(nb.sf_mma_bytes(rows, cfg.I), dtype=torch.uint8, device=DEV),
+                gs_h=torch.zeros(1, dtype=torch.float32, device=DEV),
+                slot_of=torch.zeros(cfg.T * cfg.k, dtype=torch.int32, device=DEV), path=path)
+    outs = []
+    for _ in range(2):               # a second call reuses the self-clearing counters
+        y = layer.forward(x.to(DEV), ids.to(DEV), w.to(DEV), taps=taps)
+        torch.cuda.synchronize()
+        outs.append(y.float().cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    assert layer.status() == 0
+    out = {k: v.cpu().numpy() for k, v in taps.items() if isinstance(v, torch.Tensor)}
+    out["y"] = outs[1]
+    out["row_of"] = out["slot_of"]
+    out["rows"] = rows
+    out["gs_w1"], out["gs_w2"] = g1.cpu().numpy(), g2.cpu().numpy()
+    return out
+
+
+LAYER_SMALL = syn.MoEConfig("layer16", E=8, H=512, I=256, T=16, k=4, routing="zipf")
+
+
+@pytest.mark.parametrize("cfg", [syn.CONFIGS["tiny"], LAYER_SMALL], ids=["tiny", "layer16"])
+def test_layer_kernel_matches_oracle(nb, cfg):
+    """Routing, quantisation, both GEMMs, requantisation and the reduce in
+    one cooperative kernel, against the oracle (y compared without slot_out:
+    the kernel reduces on the fly)."""
+    x = syn.draw_activations(cfg)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)])
+    g = run_gpu_layer(nb, cfg, x, ids, w, W1.to(DEV), W2.to(DEV))
+    ref = omoe.forward(x.float().numpy(), ids.numpy(), w.numpy(),
+                       *omoe.quantize_expert_weights(list(W1.numpy())),
+                       *omoe.quantize_expert_weights(list(W2.numpy())))
+    r = ref["route"]
+    p = omoe.padded_layout(r)
+    assert np.array_equal(g["slot_of"], p["row_of"])
+    dense_rows = np.empty(cfg.T * cfg.k, dtype=np.int64)
+    dense_rows[r["slot_of"]] = g["row_of"]
+    rows_close(g["l1_out"][dense_rows], ref["l1"], "l1")
+    rows_close(g["h"][dense_rows], ref["h"], "h")
+    hsf_g = unstage(g["hsf_mma"], g["rows"], cfg.I)[dense_rows]
+    check_requant(ref["h"], ref["gs_h"], ref["hq"], ref["hsf"], g["hq"][dense_rows], hsf_g)
+    rows_close(g["y"], ref["y64"], "y")
+
+
+@pytest.mark.parametrize("cfg", [syn.CONFIGS["tiny"], LAYER_SMALL], ids=["tiny", "layer16"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_layer_kernel_equals_four_calls(nb, cfg, out_dtype):
+    """The single-kernel layer and the four separate calls give the same bits."""
+    x = syn.draw_activations(cfg)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)]).to(DEV)
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)]).to(DEV)
+    a = run_gpu_layer(nb, cfg, x, ids, w, W1, W2, out_dtype=out_dtype, path=3)
+    b = run_gpu(nb, cfg, x, ids, w, W1, W2, out_dtype=out_dtype, path=1)
+    rows = b["row_of"]
+    assert np.array_equal(a["row_of"], rows)
+    for key in ("l1_out", "h", "hq"):
+        assert np.array_equal(a[key][rows], b[key][rows]), key
+    assert np.array_equal(a["gs_h"], b["gs_h"])
+    assert np.array_equal(a["y"], b["y"])
+
+
+def test_layer_forward_large_batch_uses_four_launches(nb):
+    """Above the single-kernel limits the one-call API runs the four steps."""
+    cfg = syn.CONFIGS["small"]                       # T*k = 291 > 128
+    x = syn.draw_activations(cfg)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)]).to(DEV)
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)]).to(DEV)
+    with pytest.raises(nb.NvmoeError):
+        run_gpu_layer(nb, cfg, x, ids, w, W1, W2, path=3)
+    a = run_gpu_layer(nb, cfg, x, ids, w, W1, W2, path=0)
+    b = run_gpu(nb, cfg, x, ids, w, W1, W2, path=0)
+    assert np.array_equal(a["y"], b["y"])
