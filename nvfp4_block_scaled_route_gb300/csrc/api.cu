@@ -503,7 +503,7 @@ static size_t layer_layout(int64_t T, int k, int E, int H, int I, uint8_t* base,
   b->quant_ws_bytes = nvfp4_quantize_workspace_size(T, H);
   b->quant_ws = c.take<uint8_t>(b->quant_ws_bytes);
   b->slot_out = c.take<float>(static_cast<size_t>(rows) * H * sizeof(float));
-  b->grid_bar = c.take<int>(4 * sizeof(int));
+  b->grid_bar = c.take<int>(kLayerBarWords * sizeof(int));
   b->ycnt = c.take<int>(static_cast<size_t>(T > 0 ? T : 1) * (H / 256 + 1) * sizeof(int));
   return c.off;
 }

@@ -321,13 +321,12 @@ __device__ bool grid_barrier(int* bar, int generation, int* status, volatile int
   return wait_flag(&bar[1], generation, status, abort);
 }
 
-// What the activation (A) loads of a phase wait for: a global generation
-// flag (grid barrier) or a shared-memory mbarrier completed by this CTA's
-// epilogue warps once they have written the rows the CTA needs.
+// What the activation (A) loads of a phase wait for: a global word reaching
+// `target` (a grid barrier's generation, or a count of CTAs whose share of
+// the quantised activations is written).
 struct Gate {
   const int* flag;
   int target;
-  uint64_t* bar;
 };
 
 // ------------------------------------------------------------ producer --
@@ -359,12 +358,7 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
     bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa, kSfaBytes, full, pol_a);
   };
   auto open_gate = [&]() -> bool {
-    if (gate->bar != nullptr) {
-      if (!mbar_wait(gate->bar, 0, args.status, abort)) return false;
-      fence_proxy_async_global();
-    } else if (!wait_flag(gate->flag, gate->target, args.status, abort)) {
-      return false;
-    }
+    if (!wait_flag(gate->flag, gate->target, args.status, abort)) return false;
     gate_open = true;
     for (int i = 0; i < n_def; ++i) issue_a(def_stage[i], def_row[i], def_ks[i], def_small[i]);
     n_def = 0;
@@ -881,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
   Pipe pp;
   if (warp == 0) {
     if (lane == 0) {
-      const Gate g2{&f.grid_bar[1], 2, nullptr};
+      const Gate g2{&f.grid_bar[1], 2};
       if (run_producer(P1, E, tb, bars, smem, pp, abort, nullptr))
         run_producer(P2, E, tb, bars, smem, pp, abort, &g2);
       drain_producer(bars, pp, a1.status);
@@ -919,15 +913,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
 // ------------------------------------------------------- layer kernel ----
 // The whole forward of a small batch in one cooperative launch: routing,
 // activation quantisation, L1, requantisation, L2 and the weighted reduce.
-//  * every CTA builds the routing tables itself from topk_ids (no barrier);
-//  * every CTA computes gs_x over all of x and quantises the activation rows
-//    of its own L1 m-tiles (several CTAs may write the same rows, with the
-//    same bytes), so its weight loads start at once and its activation loads
-//    only wait for its own epilogue warps;
-//  * one grid barrier after L1 (the intermediate global scale needs every h);
-//    then every CTA requantises the rows of its own L2 m-tiles;
+//  * every CTA builds the routing tables itself from topk_ids and computes
+//    gs_x over all of x (no barrier), and its weight loads start at once;
+//  * the activation blocks are quantised once, spread over the grid (each
+//    CTA a 1/G share, written to every slot row of the token); a CTA's
+//    activation loads wait for a grid-wide count of finished shares;
+//  * one grid barrier after L1 (the intermediate global scale needs every
+//    h); then h is requantised the same way, a 1/G share per CTA, and the
+//    L2 activation loads wait for the second count;
 //  * the top-k reduce of a (token, 256-column tile) is done by the CTA that
 //    writes the last of the token's k slot rows of that tile.
+// Work per CTA before each wait is one or two rounds of 16-element blocks
+// per thread: on a small batch the critical path is a handful of memory
+// round trips, not a loop over whole rows.
 struct LayerArgs {
   const __nv_bfloat16* x;     // [T, H]
   const int32_t* topk_ids;    // [T, k]
@@ -941,7 +939,8 @@ struct LayerArgs {
   int32_t* expert_counts;     // [E]
   int32_t* row_token;         // [rows]
   int32_t* slot_of;           // [T*k]
-  int* grid_bar;              // [3] arrivals, generation, exits; zero between calls
+  int* grid_bar;              // [kLayerBarWords]: barrier arrivals, generation, exits,
+                              // x shares done, h shares done; zero between calls
   int* ycnt;                  // [T * H/256], zero between calls
   uint8_t* hq;
   uint8_t* hsf;
@@ -951,84 +950,94 @@ struct LayerArgs {
 };
 
 
-// Quantise, with scale gs, the valid rows of every m-tile this CTA works on
-// in phase P (epilogue warps).  Rows come from `src` (bf16 tokens through
-// dense_token, or fp32 slot rows), go to q / staged sf of the slot layout.
+// Quantise this CTA's share of the 16-element blocks of `n_rows` source
+// rows of `cols` columns (epilogue warps, one block per thread per round),
+// with scale gs.  kFromTokens: source row t is token t of the bf16 x and its
+// blocks go to the k slot rows of the token (slot_row[t*k + j], -1 = none);
+// else source row i is flat slot i, read (fp32) from and written to slot
+// row slot_row[i].  Shares are whole groups of 4 blocks, so the 4 scale
+// bytes of a staged 32-bit word come from 4 neighbouring lanes.
 template <bool kFromTokens>
-__device__ void quantise_own_rows(const Phase& P, const Tables& tb, int E, const void* src,
-                                  int cols, const int* dense_token, uint8_t* q, uint8_t* sf,
-                                  float gs) {
+__device__ void quantise_share(const void* src, int n_rows, int cols, int k,
+                               const int* slot_row, uint8_t* q, uint8_t* sf, float gs) {
   const int bpr = cols >> 4;
   const int k_atoms = (cols + kStageK - 1) / kStageK * 4;
   const float denom = __fmul_rn(6.0f, gs);
-  const int lane = threadIdx.x & 31;
-  const int ew = (threadIdx.x >> 5) - 2;
-  WorkIter it;
-  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
-  int seen_e[4], seen_mt[4], n_seen = 0;
-  int tile, s0, s1;
-  while (it.next(tile, s0, s1)) {
-    const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
-    bool dup = false;
-    for (int i = 0; i < n_seen; ++i) dup |= seen_e[i] == ti.e && seen_mt[i] == ti.mt;
-    if (dup) continue;
-    if (n_seen < 4) {
-      seen_e[n_seen] = ti.e;
-      seen_mt[n_seen] = ti.mt;
-      ++n_seen;
-    }
-    const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
-    const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
-    const int d0 = tb.dense[ti.e] + ti.mt * kBM;
-    const int total = n_valid * bpr;
-    for (int base = ew * 32; base < total; base += 128) {      // warp-uniform
-      const int i = base + lane;
-      const bool active = i < total;
-      const int r = active ? i / bpr : 0;
-      const int g = active ? i - r * bpr : 0;
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+  const int etid = threadIdx.x - 64;
+  const int n_quads = n_rows * (bpr >> 2);
+  const int q0 = static_cast<int>(static_cast<int64_t>(n_quads) * blockIdx.x / gridDim.x);
+  const int q1 = static_cast<int>(static_cast<int64_t>(n_quads) * (blockIdx.x + 1) / gridDim.x);
+  const int b_end = 4 * q1;
+  for (int b0 = 4 * q0 + (etid & ~31); b0 < b_end; b0 += 128) {      // warp-uniform
+    const int b = b0 + (etid & 31);
+    const bool active = b < b_end;
+    const int r = active ? b / bpr : 0;
+    const int g = active ? b - r * bpr : 0;
+    float v[16];
+    int row = -1;
+    if (kFromTokens) {
+      uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
       if (active) {
-        if (kFromTokens) {
-          const int t = dense_token[d0 + r];
-          const uint4* p = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(src) + static_cast<int64_t>(t) * cols + g * 16);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint4 u = __ldg(p + c);
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              v[8 * c + 2 * m] = __uint_as_float(w4[m] << 16);
-              v[8 * c + 2 * m + 1] = __uint_as_float(w4[m] & 0xFFFF0000u);
-            }
-          }
-        } else {
-          const float4* p = reinterpret_cast<const float4*>(
-              static_cast<const float*>(src) + (row0 + r) * cols + g * 16);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float4 f = __ldcg(p + c);
-            v[4 * c] = f.x; v[4 * c + 1] = f.y; v[4 * c + 2] = f.z; v[4 * c + 3] = f.w;
-          }
-        }
+        const uint4* p = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(src) + static_cast<int64_t>(r) * cols + g * 16);
+        u0 = __ldg(p);
+        u1 = __ldg(p + 1);
       }
-      uint32_t packed[2];
-      const uint32_t s = quant_block16(v, gs, denom, packed);
-      const uint32_t sa = __shfl_down_sync(0xFFFFFFFFu, s, 1);
-      const uint32_t sb = __shfl_down_sync(0xFFFFFFFFu, s, 2);
-      const uint32_t sc = __shfl_down_sync(0xFFFFFFFFu, s, 3);
-      if (!active) continue;
-      *reinterpret_cast<uint2*>(q + (row0 + r) * (cols >> 1) + g * 8) =
+      const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        v[2 * m] = __uint_as_float(w8[m] << 16);
+        v[2 * m + 1] = __uint_as_float(w8[m] & 0xFFFF0000u);
+      }
+    } else {
+      if (active) row = slot_row[r];
+      float4 f[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row >= 0) {
+        const float4* p = reinterpret_cast<const float4*>(
+            static_cast<const float*>(src) + static_cast<int64_t>(row) * cols + g * 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) f[c] = __ldcg(p + c);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        v[4 * c] = f[c].x;
+        v[4 * c + 1] = f[c].y;
+        v[4 * c + 2] = f[c].z;
+        v[4 * c + 3] = f[c].w;
+      }
+    }
+    uint32_t packed[2];
+    const uint32_t s = quant_block16(v, gs, denom, packed);
+    const uint32_t word = s | (__shfl_down_sync(0xFFFFFFFFu, s, 1) << 8) |
+                          (__shfl_down_sync(0xFFFFFFFFu, s, 2) << 16) |
+                          (__shfl_down_sync(0xFFFFFFFFu, s, 3) << 24);
+    if (!active) continue;
+    auto put = [&](int dst) {
+      *reinterpret_cast<uint2*>(q + static_cast<int64_t>(dst) * (cols >> 1) + g * 8) =
           make_uint2(packed[0], packed[1]);
       if ((g & 3) == 0)
-        *reinterpret_cast<uint32_t*>(sf + staged_offset(row0 + r, g, k_atoms)) =
-            s | (sa << 8) | (sb << 16) | (sc << 24);
+        *reinterpret_cast<uint32_t*>(sf + staged_offset(dst, g, k_atoms)) = word;
+    };
+    if (kFromTokens) {
+      for (int j = 0; j < k; ++j) {
+        const int dst = slot_row[r * k + j];
+        if (dst >= 0) put(dst);
+      }
+    } else if (row >= 0) {
+      put(row);
     }
   }
-  // the producer's TMA reads of these rows come after this (async proxy)
+}
+
+// Publish this CTA's finished share: its writes are made visible to every
+// CTA, to the generic and the async (TMA) proxy, then counted.
+__device__ void share_done(int* count) {
   fence_proxy_async_global();
+  __threadfence();
+  epi_bar();
+  if (threadIdx.x == 64) atomicAdd(count, 1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
@@ -1045,7 +1054,6 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   __shared__ int s_tok[kLayerMaxSlots];       // token of dense slot
   __shared__ int s_scratch[kMaxExperts];      // running counts, then the reduce list
   __shared__ float s_gs;
-  __shared__ __align__(8) uint64_t s_gate[2];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a1.E, k = L.k, S = L.T * L.k;
@@ -1066,84 +1074,46 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
       record_status(a1.status, kErrBadIndex);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int off = 0, p1 = 0, p2 = 0, d = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = tb.cnt[e];
-      tb.off[e] = off;
-      tb.mtiles[e] = (c + kBM - 1) / kBM;
-      tb.prefix1[e] = p1;
-      tb.prefix2[e] = p2;
-      tb.dense[e] = d;
-      off += tb.mtiles[e] * kBM;
-      p1 += tb.mtiles[e] * a1.n_tiles;
-      p2 += tb.mtiles[e] * a2.n_tiles;
-      d += c;
-    }
-    tb.prefix1[E] = p1;
-    tb.prefix2[E] = p2;
-    tb.dense[E] = d;
-    if (blockIdx.x == 0) L.expert_offsets[E] = off;
-    mbar_init(&s_gate[0], 1);
-    mbar_init(&s_gate[1], 1);
-    fence_mbarrier_init();
-  }
-  __syncthreads();
   if (warp == 0) {
-    // stable rank inside each expert: one warp, 32 flat indices per round
-    const unsigned lt = (1u << lane) - 1u;
-    for (int base = 0; base < S; base += 32) {
-      const int i = base + lane;
-      int e = i < S ? L.topk_ids[i] : -1;
-      if (e >= E) e = -1;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-      const int rank = __popc(peers & lt);
-      const int before = e >= 0 ? s_scratch[e] : 0;
-      __syncwarp();
-      if (e >= 0 && (peers >> lane) == 1u) s_scratch[e] = before + rank + 1;
-      __syncwarp();
-      if (i < S) {
-        s_row[i] = e >= 0 ? tb.off[e] + before + rank : -1;
-        if (e >= 0) s_tok[tb.dense[e] + before + rank] = i / k;
+    // exclusive prefix sums over the experts: each lane a run of experts,
+    // then a warp scan of the run totals (slots, m-tiles)
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int c_sum = 0, m_sum = 0;
+    for (int e = e0; e < e1; ++e) {
+      c_sum += tb.cnt[e];
+      m_sum += (tb.cnt[e] + kBM - 1) / kBM;
+    }
+    int c_inc = c_sum, m_inc = m_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int c_up = __shfl_up_sync(0xFFFFFFFFu, c_inc, o);
+      const int m_up = __shfl_up_sync(0xFFFFFFFFu, m_inc, o);
+      if (lane >= o) {
+        c_inc += c_up;
+        m_inc += m_up;
       }
     }
-  }
-  // ---- gs_x = amax(x) / 2688, in every CTA ----
-  {
-    const int64_t n_vec = static_cast<int64_t>(L.T) * H / 8;
-    float m = 0.0f;
-    for (int64_t i = threadIdx.x; i < n_vec; i += blockDim.x) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(L.x) + i);
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[j] << 16)),
-                           fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+    int d = c_inc - c_sum, mt = m_inc - m_sum;
+    for (int e = e0; e < e1; ++e) {
+      const int c = tb.cnt[e];
+      const int m = (c + kBM - 1) / kBM;
+      tb.mtiles[e] = m;
+      tb.off[e] = mt * kBM;
+      tb.prefix1[e] = mt * a1.n_tiles;
+      tb.prefix2[e] = mt * a2.n_tiles;
+      tb.dense[e] = d;
+      d += c;
+      mt += m;
     }
-    m = warp_max(m);
-    // |x| >= 0, so the float bits order like the values
-    if (lane == 0) atomicMax(reinterpret_cast<int*>(&s_amax[0]), __float_as_int(m));
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      s_gs = global_scale_from(s_amax[0]);
-      if (blockIdx.x == 0) *L.gs_x = s_gs;
+    if (lane == 31) {
+      tb.prefix1[E] = m_inc * a1.n_tiles;
+      tb.prefix2[E] = m_inc * a2.n_tiles;
+      tb.dense[E] = c_inc;
+      if (blockIdx.x == 0) L.expert_offsets[E] = m_inc * kBM;
     }
   }
   __syncthreads();
-  // ---- routing outputs for the caller (CTA 0) ----
-  if (blockIdx.x == 0) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      L.expert_offsets[e] = tb.off[e];
-      L.expert_counts[e] = tb.cnt[e];
-    }
-    for (int64_t r = threadIdx.x; r < L.rows; r += blockDim.x) L.row_token[r] = -1;
-    __syncthreads();
-    for (int i = threadIdx.x; i < S; i += blockDim.x) {
-      L.slot_of[i] = s_row[i];
-      if (s_row[i] >= 0) L.row_token[s_row[i]] = i / k;
-    }
-  }
-
   const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2);
   volatile int* abort = &bars->abort;
   const Phase P1 = make_phase(a1, &map_x, &map_w1, tb.prefix1, E);
@@ -1151,8 +1121,9 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   Pipe pp;
   if (warp == 0) {
     if (lane == 0) {
-      const Gate g1{nullptr, 0, &s_gate[0]};
-      const Gate g2{nullptr, 0, &s_gate[1]};
+      const int G = static_cast<int>(gridDim.x);
+      const Gate g1{&L.grid_bar[3], G};
+      const Gate g2{&L.grid_bar[4], G};
       if (run_producer(P1, E, tb, bars, smem, pp, abort, &g1))
         run_producer(P2, E, tb, bars, smem, pp, abort, &g2);
       drain_producer(bars, pp, a1.status);
@@ -1163,10 +1134,77 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
       mma_drain(bars, a1.status);
     }
   } else {
+    // The weight loads are already going out; meanwhile the epilogue warps
+    // rank the slots, take the activations' global scale and quantise this
+    // CTA's share of the activation blocks.
     const bool lead = warp == 2 && lane == 0;
-    quantise_own_rows<true>(P1, tb, E, L.x, H, s_tok, L.xq, L.xsf, s_gs);
+    const int etid = threadIdx.x - 64;
+    if (warp == 2) {
+      // stable rank inside each expert: one warp, 32 flat indices per round
+      const unsigned lt = (1u << lane) - 1u;
+      for (int base = 0; base < S; base += 32) {
+        const int i = base + lane;
+        int e = i < S ? L.topk_ids[i] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(peers & lt);
+        const int before = e >= 0 ? s_scratch[e] : 0;
+        __syncwarp();
+        if (e >= 0 && (peers >> lane) == 1u) s_scratch[e] = before + rank + 1;
+        __syncwarp();
+        if (i < S) {
+          s_row[i] = e >= 0 ? tb.off[e] + before + rank : -1;
+          if (e >= 0) s_tok[tb.dense[e] + before + rank] = i / k;
+        }
+      }
+    }
+    {
+      // gs_x = amax(x) / 2688; the loads of a thread are issued in batches
+      const int n_vec = L.T * H / 8;
+      float m = 0.0f;
+      for (int i0 = etid; i0 < n_vec; i0 += 128 * 8) {
+        uint4 u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j * 128;
+          u[j] = i < n_vec ? __ldg(reinterpret_cast<const uint4*>(L.x) + i)
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[c] << 16)),
+                               fabsf(__uint_as_float(w4[c] & 0xFFFF0000u))));
+        }
+      }
+      m = warp_max(m);
+      // |x| >= 0, so the float bits order like the values
+      if (lane == 0) atomicMax(reinterpret_cast<int*>(&s_amax[0]), __float_as_int(m));
+    }
     epi_bar();
-    if (lead) mbar_arrive(&s_gate[0]);
+    if (lead) {
+      s_gs = global_scale_from(s_amax[0]);
+      if (blockIdx.x == 0) *L.gs_x = s_gs;
+    }
+    if (blockIdx.x == 0) {
+      // routing outputs for the caller
+      for (int e = etid; e < E; e += 128) {
+        L.expert_offsets[e] = tb.off[e];
+        L.expert_counts[e] = tb.cnt[e];
+      }
+      for (int64_t r = etid; r < L.rows; r += 128) L.row_token[r] = -1;
+    }
+    epi_bar();
+    if (blockIdx.x == 0) {
+      for (int i = etid; i < S; i += 128) {
+        L.slot_of[i] = s_row[i];
+        if (s_row[i] >= 0) L.row_token[s_row[i]] = i / k;
+      }
+    }
+    quantise_share<true>(L.x, L.T, H, k, s_row, L.xq, L.xsf, s_gs);
+    share_done(&L.grid_bar[3]);
     float amax = 0.0f;
     bool ok = run_epilogue(P1, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
     publish_amax(amax, s_amax, a1.amax_partial);
@@ -1177,15 +1215,14 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     if (ok) {
       const float gs = global_scale_from(reduce_partials(a1.amax_partial, gridDim.x));
       if (blockIdx.x == 0 && lead) *L.gs_h = gs;
-      quantise_own_rows<false>(P2, tb, E, a1.out, I, nullptr, L.hq, L.hsf, gs);
-      epi_bar();
-      if (lead) mbar_arrive(&s_gate[1]);
+      quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, gs);
+      share_done(&L.grid_bar[4]);
       YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
                  s_scratch, &s_n};
       run_epilogue(P2, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
     } else if (lead) {
-      // let the producer's bounded gate wait end instead of timing out twice
-      mbar_arrive(&s_gate[1]);
+      // the producer's wait for the h shares ends at once
+      *abort = 1;
     }
   }
   teardown_cta(bars, tmem);
@@ -1193,9 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(&L.grid_bar[2], 1) == static_cast<int>(gridDim.x) - 1) {
-      L.grid_bar[0] = 0;
-      L.grid_bar[1] = 0;
-      L.grid_bar[2] = 0;
+      for (int i = 0; i < kLayerBarWords; ++i) L.grid_bar[i] = 0;
       __threadfence();
     }
   }

@@ -98,6 +98,8 @@ int gemm_smem_bytes();
 // The whole forward of a small batch (routing .. reduce) in one cooperative
 // launch; limits: T*k <= kLayerMaxSlots, T*H <= kQuantSmallElems, bf16 x.
 constexpr int kLayerMaxSlots = 128;
+// Synchronisation words of the layer kernel (zero between calls).
+constexpr int kLayerBarWords = 8;
 struct LayerLaunch {
   const void* x;              // bf16 [T, H]
   const int32_t* topk_ids;
