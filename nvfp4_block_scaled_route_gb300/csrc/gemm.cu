@@ -261,6 +261,41 @@ __device__ __forceinline__ void epi_l2_4(float4 a, float alpha, int64_t row, int
                   __fmul_rn(alpha, a.w));
 }
 
+// The same epilogues on one column (used where a warp's few valid rows are
+// spread over its 32 lanes, one column per lane).
+__device__ __forceinline__ void epi_l1_1(float g, float u, float alpha, int64_t row, int col,
+                                         const GemmArgs& args, float& amax) {
+  const int I = args.I;
+  const float gv = __fmul_rn(alpha, g), uv = __fmul_rn(alpha, u);
+  const float hv = __fmul_rn(silu_f(gv), uv);
+  amax = fmaxf(amax, fabsf(hv));
+  args.out[row * I + col] = hv;
+  if (args.tap != nullptr) {
+    args.tap[row * (2 * I) + col] = gv;
+    args.tap[row * (2 * I) + col + I] = uv;
+  }
+}
+
+// Value v[j] of lane `src`, delivered to lane j (32 shuffles; the register
+// index is a compile-time constant in every step).
+__device__ __forceinline__ float from_lane_column(const float (&v)[32], int src) {
+  const int lane = threadIdx.x & 31;
+  float out = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float t = __shfl_sync(0xFFFFFFFFu, v[j], src);
+    if (lane == j) out = t;
+  }
+  return out;
+}
+
+// At most this many valid rows in a warp's 32-row quarter: the full-tile L1
+// epilogue (SiLU of 128 columns per row) turns each row over to the 32 lanes,
+// one column each, instead of leaving one thread to work through the row
+// alone.  Each row costs 64 shuffles per 32 columns, so this pays only for
+// a few rows; the L2 epilogue (one multiply per column) never does.
+constexpr int kNarrowRows = 4;
+
 __device__ __forceinline__ void add4(float4& a, float4 b) {
   a.x += b.x;
   a.y += b.y;
@@ -589,19 +624,34 @@ __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* 
     const int64_t row = tb.off[ti.e] + ti.mt * kBM + row_in_tile;
     const int col0 = ti.nt * (args.mode == 1 ? 128 : kBN);
     if (s0 == 0 && s1 == P.k_stages) {
-      // whole tile in this CTA: epilogue straight from TMEM
-      if (args.mode == 1) {
+      // whole tile in this CTA: epilogue straight from TMEM.  Valid rows of
+      // this warp's quarter (warp-uniform):
+      const int nv_w = min(32, max(0, tb.cnt[ti.e] - ti.mt * kBM - q * 32));
+      const int64_t qrow0 = tb.off[ti.e] + ti.mt * kBM + q * 32;
+      if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
+        // few rows (decode): each row's columns spread over the lanes
         for (int c = 0; c < 4; ++c) {
           float g[32], u[32];
           tmem_ld_f32(t_row + c * 32, g);
           tmem_ld_f32(t_row + 128 + c * 32, u);
-          if (valid) epi_l1(g, u, alpha, row, col0 + c * 32, args, amax);
+          for (int r = 0; r < nv_w; ++r)
+            epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, qrow0 + r,
+                     col0 + c * 32 + lane, args, amax);
         }
-      } else {
-        for (int c = 0; c < 8; ++c) {
-          float a[32];
-          tmem_ld_f32(t_row + c * 32, a);
-          if (valid) epi_l2(a, alpha, row, col0 + c * 32, args);
+      } else if (nv_w > 0) {
+        if (args.mode == 1) {
+          for (int c = 0; c < 4; ++c) {
+            float g[32], u[32];
+            tmem_ld_f32(t_row + c * 32, g);
+            tmem_ld_f32(t_row + 128 + c * 32, u);
+            if (valid) epi_l1(g, u, alpha, row, col0 + c * 32, args, amax);
+          }
+        } else {
+          for (int c = 0; c < 8; ++c) {
+            float a[32];
+            tmem_ld_f32(t_row + c * 32, a);
+            if (valid) epi_l2(a, alpha, row, col0 + c * 32, args);
+          }
         }
       }
       tc_fence_before();
