@@ -598,7 +598,9 @@ __device__ void y_after_tile(const YReduce& yr, const TileInfo& ti, const Tables
 
 // Four warps (128 threads, one accumulator row each).  Returns false when
 // a wait gave up; the decision is shared so all four warps leave together.
-__device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* bars,
+// gs_a is the activations' global scale, passed by value: the caller knows
+// when it is final.
+__device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb, Barriers* bars,
                              uint32_t tmem, Pipe& pp, volatile int* abort, float& amax,
                              int* s_ok, int* s_last, const YReduce* yr = nullptr) {
   const GemmArgs& args = *P.a;
@@ -609,11 +611,16 @@ __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* 
   const bool lead = warp == 2 && lane == 0;
   WorkIter it;
   it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
-  const float gs_a = __ldcg(args.gs_a);
   int tile, s0, s1;
-  while (it.next(tile, s0, s1)) {
+  bool have = it.next(tile, s0, s1);
+  // the weight scale of the next tile is loaded one tile ahead
+  float gs_b = have ? __ldg(args.gs_b + decode_tile(tile, P.prefix, tb.mtiles, E).e) : 0.0f;
+  while (have) {
     const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
-    const float alpha = __fmul_rn(gs_a, args.gs_b[ti.e]);
+    const float alpha = __fmul_rn(gs_a, gs_b);
+    int n_tile, n_s0, n_s1;
+    const bool n_have = it.next(n_tile, n_s0, n_s1);
+    if (n_have) gs_b = __ldg(args.gs_b + decode_tile(n_tile, P.prefix, tb.mtiles, E).e);
     // one thread waits (bounded) and the decision is shared, so the four
     // epilogue warps always take the same path through the named barriers
     if (lead) *s_ok = mbar_wait(&bars->acc_full, pp.acc_phase, args.status, abort) ? 1 : 0;
@@ -725,6 +732,10 @@ __device__ bool run_epilogue(const Phase& P, int E, const Tables& tb, Barriers* 
       }
     }
     pp.acc_phase ^= 1u;
+    tile = n_tile;
+    s0 = n_s0;
+    s1 = n_s1;
+    have = n_have;
   }
   return true;
 }
@@ -843,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     }
   } else {
     float amax = 0.0f;
-    run_epilogue(P, args.E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    run_epilogue(P, __ldcg(args.gs_a), args.E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
     if (args.mode == 1) publish_amax(amax, s_amax, args.amax_partial);
   }
   teardown_cta(bars, tmem);
@@ -937,7 +948,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
     }
   } else {
     float amax = 0.0f;
-    bool ok = run_epilogue(P1, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    bool ok = run_epilogue(P1, __ldcg(a1.gs_a), E, tb, bars, tmem, pp, abort, amax, &s_ok,
+                           &s_last);
     publish_amax(amax, s_amax, a1.amax_partial);
     // barrier 1: every h row and every per-CTA amax is written
     if (warp == 2 && lane == 0)
@@ -955,7 +967,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
       epi_bar();
       ok = s_ok != 0;
     }
-    if (ok) run_epilogue(P2, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    // gs_h is final: the requantisation before the second barrier wrote it
+    if (ok)
+      run_epilogue(P2, __ldcg(a2.gs_a), E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
   }
   teardown_cta(bars, tmem);
 }
@@ -1256,7 +1270,9 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     quantise_share<true>(L.x, L.T, H, k, s_row, L.xq, L.xsf, s_gs);
     share_done(&L.grid_bar[3]);
     float amax = 0.0f;
-    bool ok = run_epilogue(P1, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
+    // every CTA computed the same gs_x itself (CTA 0's copy in memory is for
+    // the caller, with no ordering against this read)
+    bool ok = run_epilogue(P1, s_gs, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
     publish_amax(amax, s_amax, a1.amax_partial);
     // the one grid barrier: every h row and every per-CTA amax is written
     if (lead) s_ok = ok && grid_barrier(L.grid_bar, 1, a1.status, abort) ? 1 : 0;
@@ -1269,7 +1285,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
       share_done(&L.grid_bar[4]);
       YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
                  s_scratch, &s_n};
-      run_epilogue(P2, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
+      run_epilogue(P2, gs, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
     } else if (lead) {
       // the producer's wait for the h shares ends at once
       *abort = 1;
