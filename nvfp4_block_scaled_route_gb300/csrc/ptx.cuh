@@ -248,6 +248,15 @@ __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// One 32-byte store of 8 floats (p 32-byte aligned): a whole L2 sector per
+// thread instead of two half-sector writes.
+__device__ __forceinline__ void st_global_v8(float* p, const float (&v)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+                 "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 // ---------------------------------------------------------- conversions ----
 // E4M3 (satfinite, round to nearest even) of a non-negative float.
 __device__ __forceinline__ uint32_t cvt_e4m3_satfinite(float v) {
