@@ -136,6 +136,9 @@ class ClockSampler:
 
 
 # ------------------------------------------------------- oracle sample ----
+_SAMPLE_CACHE = {}
+
+
 def _oracle_sample_worker(args):
     """Time the oracle on `n_slots` slots of one token, each restricted to `c`
     of the I intermediate columns (L1: c gate + c up columns; L2: c of the I
@@ -149,14 +152,21 @@ def _oracle_sample_worker(args):
     from nvfp4_block_scaled_route_gb300 import synthetic as syn
     cfg = syn.CONFIGS[cfgname]
     H, I = cfg.H, cfg.I
-    g = torch.Generator().manual_seed(seed)
-    x = syn.draw_activations(cfg, T=1).float().numpy()
-    slots = []
-    for s in range(n_slots):
-        std = cfg.w_std * (0.5 + 1.5 * float(torch.rand(1, generator=g)))
-        w1 = (torch.randn((H, 2 * c), generator=g) * std).numpy()
-        w2 = (torch.randn((c, H), generator=g) * std).numpy()
-        slots.append((onv.quantize_weight(w1), onv.quantize_weight(w2)))
+    # the sample's weights are drawn and quantised once per (workload, slice)
+    # and kept by the worker: that set-up is not the oracle's forward work
+    key = (cfgname, c, n_slots)
+    if key not in _SAMPLE_CACHE:
+        g = torch.Generator().manual_seed(seed)
+        x = syn.draw_activations(cfg, T=1).float().numpy()
+        slots = []
+        for s in range(n_slots):
+            std = cfg.w_std * (0.5 + 1.5 * float(torch.rand(1, generator=g)))
+            w1 = (torch.randn((H, 2 * c), generator=g) * std).numpy()
+            w2 = (torch.randn((c, H), generator=g) * std).numpy()
+            slots.append((onv.quantize_weight(w1), onv.quantize_weight(w2)))
+        _SAMPLE_CACHE.clear()
+        _SAMPLE_CACHE[key] = (x, slots)
+    x, slots = _SAMPLE_CACHE[key]
     t0 = time.perf_counter()
     xq, xsf, gsx = onv.quantize_rows(x)
     y = np.zeros((1, H))
