@@ -29,10 +29,24 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float gs
   const float d = __fmul_rn(e4m3_to_float(sf), gs);
   packed[0] = packed[1] = 0u;
   if (d != 0.0f) {
+    // |v| / d correctly rounded without 16 divisions: with rd = RN(1/d),
+    // q0 = RN(|v|*rd) is within an ulp of the quotient, the residual
+    // |v| - q0*d is exact in one fma, and RN(q0 + residual*rd) is the
+    // correctly rounded quotient (Markstein's correction step, IBM J. Res.
+    // Dev. 34(1), 1990).  It needs normal numbers, which holds wherever the
+    // E2M1 decision can change (quotients >= 0.25); a divisor whose
+    // reciprocal would not be normal takes true divisions.
+    const float rd = __frcp_rn(d);
+    const bool normal = d > 1.0e-36f && d < 1.0e36f;
+    auto quot = [&](float a) {
+      if (!normal) return __fdiv_rn(a, d);
+      const float q0 = __fmul_rn(a, rd);
+      return __fmaf_rn(__fmaf_rn(-q0, d, a), rd, q0);
+    };
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       const float lo = v[2 * p], hi = v[2 * p + 1];
-      uint32_t byte = cvt_e2m1x2_satfinite(__fdiv_rn(fabsf(lo), d), __fdiv_rn(fabsf(hi), d));
+      uint32_t byte = cvt_e2m1x2_satfinite(quot(fabsf(lo)), quot(fabsf(hi)));
       byte |= (__float_as_uint(lo) >> 31) << 3;
       byte |= (__float_as_uint(hi) >> 31) << 7;
       packed[p >> 2] |= byte << (8 * (p & 3));

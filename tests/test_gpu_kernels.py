@@ -74,6 +74,63 @@ def test_quantize_act_bit_exact(nb, rows, cols, dist, dtype):
     assert np.array_equal(unstage(sf_mma.cpu().numpy(), rows, cols), xsf)
 
 
+def _bf16_bits(v: float) -> int:
+    return int(torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+
+
+@pytest.mark.parametrize("amax", [1344.0, 3.0, 2.6875])
+def test_quantize_every_bf16_against_every_scale(nb, amax):
+    """Every positive bf16 magnitude in [m/64, m], both signs, in blocks whose
+    maximum m sets each of the 126 non-zero scale bytes (global amax fixed,
+    so gs = amax/2688): nibbles and scales bit-exact against the oracle's
+    true division (the kernels divide by a reciprocal plus a correction
+    step)."""
+    gs = float(onv.global_scale(np.float32(amax)))
+    top = _bf16_bits(amax)
+    blocks = [[top] * 16]                            # fixes the global amax
+    for s in range(1, 127):
+        m = float(onv.e4m3_decode(np.array([s], dtype=np.uint8))[0]) * 6.0 * gs
+        hi = _bf16_bits(m)
+        lo = _bf16_bits(m / 64.0)
+        if hi == 0 or hi > top:
+            continue
+        vals = list(range(lo, hi + 1))
+        for c0 in range(0, len(vals), 15):
+            chunk = vals[c0:c0 + 15]
+            chunk += [hi] * (15 - len(chunk))
+            blocks.append([b | (0x8000 if i % 2 else 0) for i, b in enumerate([hi] + chunk)])
+    cols = 1024
+    while len(blocks) % (cols // 16):
+        blocks.append([0] * 16)
+    bits = np.asarray(blocks, dtype=np.uint16).reshape(-1, cols)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    rows = x.shape[0]
+    q, sf_row, sf_mma, gsg = nb.quantize_act(x.to(DEV))
+    torch.cuda.synchronize()
+    xq, xsf, xgs = onv.quantize_rows(x.float().numpy())
+    assert float(xgs) == np.float32(gs)
+    assert gsg.item() == float(xgs)
+    assert len(set(xsf.reshape(-1).tolist())) > 100          # scales really spread
+    assert np.array_equal(sf_row.cpu().numpy(), xsf)
+    assert np.array_equal(q.cpu().numpy(), xq)
+    assert np.array_equal(unstage(sf_mma.cpu().numpy(), rows, cols), xsf)
+
+
+def test_quantize_fp32_large_random(nb):
+    """12.6 M heavy-tailed fp32 values (the requantisation's input type):
+    bit-exact against the oracle."""
+    g = torch.Generator().manual_seed(11)
+    rows, cols = 4096, 3072
+    x = torch.randn((rows, cols), generator=g)
+    x = x / torch.sqrt((torch.randn((3, rows, cols), generator=g) ** 2).sum(0) / 3)
+    q, sf_row, _, gs = nb.quantize_act(x.to(DEV))
+    torch.cuda.synchronize()
+    xq, xsf, xgs = onv.quantize_rows(x.numpy())
+    assert gs.item() == float(xgs)
+    assert np.array_equal(sf_row.cpu().numpy(), xsf)
+    assert np.array_equal(q.cpu().numpy(), xq)
+
+
 def test_quantize_act_ties_and_signs(nb):
     """Blocks whose values sit exactly on E2M1 rounding ties, saturation and
     negative values that round to zero."""
