@@ -361,6 +361,18 @@ __device__ bool grid_barrier(int* bar, int generation, int* status, volatile int
   return wait_flag(&bar[1], generation, status, abort);
 }
 
+// Grid-wide barrier of one use per launch, called by one thread per CTA:
+// arrive on the counter, then wait for it to reach the grid size (no flag
+// to publish, so the last arriver adds no round trip).  Everything this
+// CTA wrote before the call is visible to every CTA after it, to the
+// generic and the async (TMA) proxy.
+__device__ bool count_barrier(int* count, int* status, volatile int* abort) {
+  fence_proxy_async_global();
+  __threadfence();
+  atomicAdd(count, 1);
+  return wait_flag(count, static_cast<int>(gridDim.x), status, abort);
+}
+
 // What the activation (A) loads of a phase wait for: a global word reaching
 // `target` (a grid barrier's generation, or a count of CTAs whose share of
 // the quantised activations is written).
@@ -1008,8 +1020,9 @@ struct LayerArgs {
   int32_t* expert_counts;     // [E]
   int32_t* row_token;         // [rows]
   int32_t* slot_of;           // [T*k]
-  int* grid_bar;              // [kLayerBarWords]: barrier arrivals, generation, exits,
-                              // x shares done, h shares done; zero between calls
+  int* grid_bar;              // [kLayerBarWords]: barrier arrivals, (unused), exits,
+                              // x shares done, h shares done, max |h| bits;
+                              // zero between calls
   int* ycnt;                  // [T * H/256], zero between calls
   uint8_t* hq;
   uint8_t* hsf;
@@ -1279,12 +1292,20 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     // the caller, with no ordering against this read)
     bool ok = run_epilogue(P1, s_gs, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
     publish_amax(amax, s_amax, a1.amax_partial);
-    // the one grid barrier: every h row and every per-CTA amax is written
-    if (lead) s_ok = ok && grid_barrier(L.grid_bar, 1, a1.status, abort) ? 1 : 0;
+    // the one grid barrier: every h row is written and every CTA's max of |h|
+    // is folded into one word (non-negative floats order like their bits)
+    if (lead) {
+      s_ok = 0;
+      if (ok) {
+        const float cta_max = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
+        atomicMax(&L.grid_bar[5], __float_as_int(cta_max));
+        s_ok = count_barrier(&L.grid_bar[0], a1.status, abort) ? 1 : 0;
+      }
+    }
     epi_bar();
     ok = s_ok != 0;
     if (ok) {
-      const float gs = global_scale_from(reduce_partials(a1.amax_partial, gridDim.x));
+      const float gs = global_scale_from(__int_as_float(ld_acquire(&L.grid_bar[5])));
       if (blockIdx.x == 0 && lead) *L.gs_h = gs;
       quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, gs);
       share_done(&L.grid_bar[4]);
