@@ -224,6 +224,12 @@ int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt,
  *   w2     B tiles of the [E*H, I] matrix;  w2_sf staged,
  *          nvfp4_sf_mma_bytes(E*H, I);
  *   gs_w2  float [E]
+ *   gs_w1_up  float [E] or NULL.  Checkpoints that quantise gate_proj and
+ *          up_proj separately carry one global scale per half ("NVFP4
+ *          MegaMoE Debug Log", code-review point 5, gate/up correction:
+ *          equivalent to a per-column alpha).  When given, the gate columns
+ *          use alpha = gs_x * gs_w1[e] and the up columns alpha = gs_x *
+ *          gs_w1_up[e]; when NULL both halves use gs_w1[e].
  */
 typedef struct {
   int E, H, I;
@@ -233,6 +239,7 @@ typedef struct {
   const uint8_t* w2;
   const uint8_t* w2_sf;
   const float* gs_w2;
+  const float* gs_w1_up;
 } nvmoe_weights;
 
 /* Optional outputs of intermediate results (any member may be NULL).
@@ -270,6 +277,7 @@ typedef struct {
 /* moe_nvfp4_forward — the expert FFN on grouped slots ("NVFP4 MegaMoE Debug
  * Log", NVFP4 MoE Pipeline; Hypotheses §3 for alpha):
  *   l1[r, :]  = (gs_x * gs_w1[e]) * sum_k dec(xq) dec(xsf) dec(w1) dec(w1_sf)
+ *               (up columns: gs_w1_up[e] in place of gs_w1[e] when given)
  *   h[r, c]   = silu(l1[r, c]) * l1[r, I + c]          (fp32)
  *   hq, hsf, gs_h = step-2 quantisation of h over all valid rows
  *   out[r, :] = (gs_h * gs_w2[e]) * sum_k dec(hq) dec(hsf) dec(w2) dec(w2_sf)

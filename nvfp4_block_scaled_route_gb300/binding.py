@@ -33,7 +33,8 @@ class NvmoeError(RuntimeError):
 class Weights(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("w1", ctypes.c_void_p), ("w1_sf", ctypes.c_void_p), ("gs_w1", ctypes.c_void_p),
-                ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("gs_w2", ctypes.c_void_p)]
+                ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("gs_w2", ctypes.c_void_p),
+                ("gs_w1_up", ctypes.c_void_p)]
 
 
 class Taps(ctypes.Structure):
@@ -223,23 +224,29 @@ class PreparedWeights:
     w2: torch.Tensor
     w2_sf: torch.Tensor
     gs_w2: torch.Tensor
+    gs_w1_up: Optional[torch.Tensor] = None
 
     def struct(self) -> Weights:
         return Weights(self.E, self.H, self.I, _ptr(self.w1), _ptr(self.w1_sf), _ptr(self.gs_w1),
-                       _ptr(self.w2), _ptr(self.w2_sf), _ptr(self.gs_w2))
+                       _ptr(self.w2), _ptr(self.w2_sf), _ptr(self.gs_w2), _ptr(self.gs_w1_up))
 
     @staticmethod
-    def from_checkpoint(w1q, w1sf, gs1, w2q, w2sf, gs2) -> "PreparedWeights":
-        """w1q (E, H/2, 2I), w1sf (E, H/16, 2I), w2q (E, I/2, H), w2sf (E, I/16, H)."""
+    def from_checkpoint(w1q, w1sf, gs1, w2q, w2sf, gs2, gs1_up=None) -> "PreparedWeights":
+        """w1q (E, H/2, 2I), w1sf (E, H/16, 2I), w2q (E, I/2, H), w2sf (E, I/16, H);
+        gs1_up (E,) when the checkpoint quantised gate and up separately
+        (then gs1 is the gate half's scale)."""
         E, H2, N1 = w1q.shape
         q1, s1 = prepare_weights(w1q, w1sf)
         q2, s2 = prepare_weights(w2q, w2sf)
         return PreparedWeights(E, 2 * H2, N1 // 2, q1, s1, gs1.contiguous(), q2, s2,
-                               gs2.contiguous())
+                               gs2.contiguous(),
+                               gs1_up.contiguous() if gs1_up is not None else None)
 
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in
-                   (self.w1, self.w1_sf, self.gs_w1, self.w2, self.w2_sf, self.gs_w2))
+        ts = [self.w1, self.w1_sf, self.gs_w1, self.w2, self.w2_sf, self.gs_w2]
+        if self.gs_w1_up is not None:
+            ts.append(self.gs_w1_up)
+        return sum(t.numel() * t.element_size() for t in ts)
 
 
 # ------------------------------------------------------------- steps 3-6 --

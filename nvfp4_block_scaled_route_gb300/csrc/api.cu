@@ -373,6 +373,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a1.b_sf = w->w1_sf;
   a1.gs_a = gs_x;
   a1.gs_b = w->gs_w1;
+  a1.gs_b_up = w->gs_w1_up;
   a1.out = b.h;
   a1.tap = tap_l1;
   a1.amax_partial = b.amax;

@@ -201,7 +201,8 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + _
 
 // L1 epilogue on 32 columns: gate g[] and up u[] (raw accumulators).
 __device__ __forceinline__ void epi_l1(const float (&g)[32], const float (&u)[32], float alpha,
-                                       int64_t row, int col, const GemmArgs& args, float& amax) {
+                                       float alpha_u, int64_t row, int col, const GemmArgs& args,
+                                       float& amax) {
   const int I = args.I;
   float* hp = args.out + row * I + col;
 #pragma unroll
@@ -210,7 +211,7 @@ __device__ __forceinline__ void epi_l1(const float (&g)[32], const float (&u)[32
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       gv[j] = __fmul_rn(alpha, g[i + j]);
-      uv[j] = __fmul_rn(alpha, u[i + j]);
+      uv[j] = __fmul_rn(alpha_u, u[i + j]);
       hv[j] = __fmul_rn(silu_f(gv[j]), uv[j]);
       amax = fmaxf(amax, fabsf(hv[j]));
     }
@@ -238,13 +239,14 @@ __device__ __forceinline__ void epi_l2(const float (&a)[32], float alpha, int64_
 
 // The same epilogues on 4 columns (used by the split-tile fixup, where the
 // 128 epilogue threads share the valid rows' columns).
-__device__ __forceinline__ void epi_l1_4(float4 g, float4 u, float alpha, int64_t row, int col,
-                                         const GemmArgs& args, float& amax) {
+__device__ __forceinline__ void epi_l1_4(float4 g, float4 u, float alpha, float alpha_u,
+                                         int64_t row, int col, const GemmArgs& args,
+                                         float& amax) {
   const int I = args.I;
   const float gv[4] = {__fmul_rn(alpha, g.x), __fmul_rn(alpha, g.y), __fmul_rn(alpha, g.z),
                        __fmul_rn(alpha, g.w)};
-  const float uv[4] = {__fmul_rn(alpha, u.x), __fmul_rn(alpha, u.y), __fmul_rn(alpha, u.z),
-                       __fmul_rn(alpha, u.w)};
+  const float uv[4] = {__fmul_rn(alpha_u, u.x), __fmul_rn(alpha_u, u.y), __fmul_rn(alpha_u, u.z),
+                       __fmul_rn(alpha_u, u.w)};
   float hv[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -268,10 +270,11 @@ __device__ __forceinline__ void epi_l2_4(float4 a, float alpha, int64_t row, int
 
 // The same epilogues on one column (used where a warp's few valid rows are
 // spread over its 32 lanes, one column per lane).
-__device__ __forceinline__ void epi_l1_1(float g, float u, float alpha, int64_t row, int col,
-                                         const GemmArgs& args, float& amax) {
+__device__ __forceinline__ void epi_l1_1(float g, float u, float alpha, float alpha_u,
+                                         int64_t row, int col, const GemmArgs& args,
+                                         float& amax) {
   const int I = args.I;
-  const float gv = __fmul_rn(alpha, g), uv = __fmul_rn(alpha, u);
+  const float gv = __fmul_rn(alpha, g), uv = __fmul_rn(alpha_u, u);
   const float hv = __fmul_rn(silu_f(gv), uv);
   amax = fmaxf(amax, fabsf(hv));
   args.out[row * I + col] = hv;
@@ -630,14 +633,23 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
   it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
   int tile, s0, s1;
   bool have = it.next(tile, s0, s1);
-  // the weight scale of the next tile is loaded one tile ahead
-  float gs_b = have ? __ldg(args.gs_b + decode_tile(tile, P.prefix, tb.mtiles, E).e) : 0.0f;
+  // the weight scales of the next tile are loaded one tile ahead; the up
+  // half of L1 has its own scale when the checkpoint gives one
+  const float* gs_b_up = args.gs_b_up != nullptr ? args.gs_b_up : args.gs_b;
+  int e0 = have ? decode_tile(tile, P.prefix, tb.mtiles, E).e : 0;
+  float gs_b = have ? __ldg(args.gs_b + e0) : 0.0f;
+  float gs_u = have ? __ldg(gs_b_up + e0) : 0.0f;
   while (have) {
     const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
     const float alpha = __fmul_rn(gs_a, gs_b);
+    const float alpha_u = __fmul_rn(gs_a, gs_u);
     int n_tile, n_s0, n_s1;
     const bool n_have = it.next(n_tile, n_s0, n_s1);
-    if (n_have) gs_b = __ldg(args.gs_b + decode_tile(n_tile, P.prefix, tb.mtiles, E).e);
+    if (n_have) {
+      const int ne = decode_tile(n_tile, P.prefix, tb.mtiles, E).e;
+      gs_b = __ldg(args.gs_b + ne);
+      gs_u = __ldg(gs_b_up + ne);
+    }
     // one thread waits (bounded) and the decision is shared, so the four
     // epilogue warps always take the same path through the named barriers
     if (lead) *s_ok = mbar_wait(&bars->acc_full, pp.acc_phase, args.status, abort) ? 1 : 0;
@@ -659,7 +671,7 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
           tmem_ld_f32(t_row + c * 32, g);
           tmem_ld_f32(t_row + 128 + c * 32, u);
           for (int r = 0; r < nv_w; ++r)
-            epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, qrow0 + r,
+            epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u, qrow0 + r,
                      col0 + c * 32 + lane, args, amax);
         }
       } else if (nv_w > 0) {
@@ -668,7 +680,7 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
             float g[32], u[32];
             tmem_ld_f32(t_row + c * 32, g);
             tmem_ld_f32(t_row + 128 + c * 32, u);
-            if (valid) epi_l1(g, u, alpha, row, col0 + c * 32, args, amax);
+            if (valid) epi_l1(g, u, alpha, alpha_u, row, col0 + c * 32, args, amax);
           }
         } else {
           for (int c = 0; c < 8; ++c) {
@@ -741,7 +753,7 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
             }
           }
           if (args.mode == 1)
-            epi_l1_4(a, b, alpha, row0 + r, col0 + g4 * 4, args, amax);
+            epi_l1_4(a, b, alpha, alpha_u, row0 + r, col0 + g4 * 4, args, amax);
           else
             epi_l2_4(a, alpha, row0 + r, col0 + g4 * 4, args);
         }

@@ -73,6 +73,7 @@ struct GemmArgs {
   const uint8_t* b_sf;    // staged, E*N x K
   const float* gs_a;      // [1]
   const float* gs_b;      // [E]
+  const float* gs_b_up;   // L1: [E] scale of the up half, or null (= gs_b)
   float* out;             // L1: h [rows, I]; L2: slot_out [rows, N]
   float* tap;             // L1: l1_out [rows, 2I] or null
   float* amax_partial;    // L1: [grid]

@@ -19,7 +19,7 @@ interleave): gate = columns [0, I), up = columns [I, 2I).
 
 Accumulation is fp64 throughout; h is rounded to fp32 before it is
 requantised (it is an fp32 tensor in the pipeline); y is rounded once to
-bf16.  Readings where the pages are silent are listed in the design doc.
+bf16.
 """
 from __future__ import annotations
 
@@ -106,9 +106,21 @@ def silu(x: np.ndarray) -> np.ndarray:
 
 
 def expert_l1(a_q, a_sf, gs_a, w1_q, w1_sf, gs_w1):
-    """Alpha-scaled L1 output [M, 2I] (fp64): acc * (gs_a * gs_w1)."""
-    alpha = float(np.float32(gs_a)) * float(np.float32(gs_w1))
-    return block_scaled_matmul(a_q, a_sf, w1_q, w1_sf) * alpha
+    """Alpha-scaled L1 output [M, 2I] (fp64): acc * (gs_a * gs_w1).
+
+    gs_w1 is one scalar, or a (gate, up) pair for checkpoints that quantise
+    the two halves separately: then the gate columns [0, I) take
+    gs_a * gs_gate and the up columns [I, 2I) gs_a * gs_up (the Debug Log's
+    gate/up correction, code-review point 5: a per-column alpha)."""
+    acc = block_scaled_matmul(a_q, a_sf, w1_q, w1_sf)
+    g = np.atleast_1d(np.asarray(gs_w1, dtype=np.float32))
+    if g.size == 1:
+        return acc * (float(np.float32(gs_a)) * float(g[0]))
+    I = acc.shape[1] // 2
+    out = np.empty_like(acc)
+    out[:, :I] = acc[:, :I] * (float(np.float32(gs_a)) * float(g[0]))
+    out[:, I:] = acc[:, I:] * (float(np.float32(gs_a)) * float(g[1]))
+    return out
 
 
 def swiglu(l1: np.ndarray) -> np.ndarray:
@@ -139,12 +151,24 @@ def unpermute_reduce(slot_out: np.ndarray, slot_of: np.ndarray, topk_w: np.ndarr
 
 # -------------------------------------------------------------- forward ----
 
-def quantize_expert_weights(w_list):
+def quantize_expert_weights(w_list, split_halves: bool = False):
     """List of fp32 (K, N) weights -> stacked checkpoint tensors
-    (E, K/2, N), (E, K/16, N), gs (E,) float32."""
+    (E, K/2, N), (E, K/16, N), gs (E,) float32.
+
+    split_halves: the columns [0, N/2) and [N/2, N) (L1 gate and up) are
+    quantised as two separate matrices with their own global scales, and gs
+    is (E, 2) float32 (gate, up)."""
     qs, sfs, gss = [], [], []
     for w in w_list:
-        q, sf, gs = nvfp4.quantize_weight(w)
+        if split_halves:
+            n = w.shape[1] // 2
+            qg, sfg, gg = nvfp4.quantize_weight(w[:, :n])
+            qu, sfu, gu = nvfp4.quantize_weight(w[:, n:])
+            q = np.concatenate([qg, qu], axis=1)
+            sf = np.concatenate([sfg, sfu], axis=1)
+            gs = (gg, gu)
+        else:
+            q, sf, gs = nvfp4.quantize_weight(w)
         qs.append(q)
         sfs.append(sf)
         gss.append(gs)
@@ -156,7 +180,8 @@ def forward(x, topk_ids, topk_w, w1_q, w1_sf, gs_w1, w2_q, w2_sf, gs_w2,
     """Whole forward pass.  x: [T, H] float32 holding bf16 values.
 
     Weights in checkpoint layout: w1_q (E, H/2, 2I), w1_sf (E, H/16, 2I),
-    w2_q (E, I/2, H), w2_sf (E, I/16, H), gs_w* (E,).  w*_q may also be a
+    w2_q (E, I/2, H), w2_sf (E, I/16, H), gs_w* (E,); gs_w1 may be (E, 2)
+    (separate gate and up global scales).  w*_q may also be a
     callable e -> (q, sf) that yields one expert at a time (to bound memory).
     Returns a dict of every intermediate (dense slot order).
     """

@@ -16,7 +16,7 @@ Sources (web pages of the NVFP4 MegaMoE kernel debug effort):
   1.875 under the OCP E4M3 definition used here (bias 7, no infinities,
   0x7F/0xFF NaN, max 448).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * rounding is nearest, ties to the even mantissa (code with bit 0 clear);
 * encoders saturate to the largest finite value (6 for E2M1, 448 for E4M3);

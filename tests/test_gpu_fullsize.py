@@ -16,7 +16,9 @@ through requantisation, L2 and the top-k reduce.  Checked:
   weight global scales    bit-exact
   sampled h rows          max|err| <= 2e-3 * row-amax, cosine >= 0.9999
   sampled hq / hsf        bit-exact except on rounding boundaries
-  sampled y (bf16)        2e-3 * row-amax plus one bf16 rounding
+  sampled y (bf16)        2e-3 * row-amax plus one bf16 rounding (where a
+                          requantised value sat on a rounding boundary, the
+                          oracle follows the GPU's decision there)
   y with and without the intermediate taps: identical bits
 """
 import numpy as np
@@ -141,6 +143,10 @@ def test_full_size_sampled_tokens(nb, name):
     rows_close(h_gpu, h_ref, "h")
     hq_ref, hsf_ref, _ = onv.quantize_rows(h_ref, gs_h)
     flips = check_requant(h_ref, gs_h, hq_ref, hsf_ref, hq_gpu, hsf_gpu)
+    if sum(flips):
+        # every difference lies on a rounding boundary, where both decisions
+        # are correct: follow the decision the GPU took
+        hq_ref, hsf_ref = hq_gpu, hsf_gpu
     y64 = np.zeros((len(sample), H), dtype=np.float64)
     for a, t in enumerate(sample):
         for j in range(k):

@@ -426,6 +426,47 @@ def test_alpha_is_linear_per_expert():
     assert np.array_equal(moe.expert_l1(aq, asf, np.float32(4 * gs_a), wq, wsf, gs_w), 4 * base)
 
 
+def test_gate_up_scales_per_column_alpha():
+    """Separate gate/up global scales (Debug Log, code-review point 5): the
+    up half scales with gs_up alone, the gate half with gs_gate alone, and
+    the per-column alpha equals the pages' correction up *= gs_up / gs_gate
+    applied on top of one alpha."""
+    rng = np.random.default_rng(10)
+    aq, asf, gs_a = _rand_nvfp4(rng, 3, 64)
+    wq, wsf, gs_w = nvfp4.quantize_weight(rng.normal(0, 1, (64, 8)).astype(np.float32))
+    one = moe.expert_l1(aq, asf, gs_a, wq, wsf, gs_w)
+    same = moe.expert_l1(aq, asf, gs_a, wq, wsf, (gs_w, gs_w))
+    assert np.array_equal(one, same)
+    pair = moe.expert_l1(aq, asf, gs_a, wq, wsf, (gs_w, np.float32(2 * gs_w)))
+    assert np.array_equal(pair[:, :4], one[:, :4])
+    assert np.array_equal(pair[:, 4:], 2 * one[:, 4:])
+    g_gate, g_up = np.float32(gs_w), np.float32(0.37 * gs_w)
+    pc = moe.expert_l1(aq, asf, gs_a, wq, wsf, (g_gate, g_up))
+    corrected = moe.expert_l1(aq, asf, gs_a, wq, wsf, g_gate)
+    corrected[:, 4:] *= float(g_up) / float(g_gate)
+    assert np.allclose(pc, corrected, rtol=1e-13, atol=0)
+
+
+def test_split_halves_quantisation():
+    """Quantising [gate | up] as two matrices: each half equals quantising it
+    alone; with equal half maxima it equals the joint quantisation."""
+    rng = np.random.default_rng(12)
+    g = rng.normal(0, 1, (64, 8)).astype(np.float32)
+    u = rng.normal(0, 3, (64, 8)).astype(np.float32)
+    q, sf, gs = moe.quantize_expert_weights([np.concatenate([g, u], 1)], split_halves=True)
+    qg, sfg, gg = nvfp4.quantize_weight(g)
+    qu, sfu, gu = nvfp4.quantize_weight(u)
+    assert gs.shape == (1, 2) and gs[0, 0] == gg and gs[0, 1] == gu
+    assert np.array_equal(q[0], np.concatenate([qg, qu], 1))
+    assert np.array_equal(sf[0], np.concatenate([sfg, sfu], 1))
+    u2 = u / np.abs(u).max() * np.abs(g).max()       # same maximum in both halves
+    w = np.concatenate([g, u2.astype(np.float32)], 1)
+    qs, sfs, gss = moe.quantize_expert_weights([w], split_halves=True)
+    qj, sfj, gj = moe.quantize_expert_weights([w])
+    assert gss[0, 0] == gss[0, 1] == gj[0]
+    assert np.array_equal(qs, qj) and np.array_equal(sfs, sfj)
+
+
 def test_silu_closed_forms():
     x = np.array([-30.0, -2.0, -0.5, 0.0, 0.5, 1.0, 3.0, 40.0])
     s = moe.silu(x)
