@@ -61,6 +61,10 @@ def parse():
     p.add_argument("--config", default="decode1")
     p.add_argument("--api", choices=["layer", "calls"], default="layer",
                    help="one-call layer entry point, or route/quantise/forward/reduce")
+    p.add_argument("--gate-up-scales", choices=["joint", "split"], default="joint",
+                   help="one L1 weight global scale per expert, or separate gate/up scales")
+    p.add_argument("--part", choices=["layer", "router"], default="layer",
+                   help="the MoE layer (steps 1-7), or the router front-end alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
@@ -258,6 +262,53 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_router(args, nb, syn, cfg, dev, world, torch):
+    """The router front-end alone (moe_router_topk) on the workload's tokens:
+    logits over the E experts, top-k, softmax; one CUDA graph per step, L2
+    flushed before every step."""
+    x = syn.draw_activations(cfg).to(dev)
+    w = syn.draw_router_weight(cfg).to(dev)
+    mode = nb.ROUTER_ALL if cfg.routing == "softmax_topk_probs" else nb.ROUTER_SELECTED
+    ws = nb._workspace(nb.lib().moe_router_workspace_size(cfg.T, cfg.H, cfg.E), dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            nb.router_topk(x, w, cfg.k, mode, ws=ws)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        nb.router_topk(x, w, cfg.k, mode, ws=ws)
+    times = []
+    with torch.cuda.stream(stream):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.warmup + args.steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    stream.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs[args.warmup:]]
+    ms = sum(times) / len(times)
+    nbytes = x.nbytes + w.nbytes + cfg.T * cfg.k * 8
+    flops = 2.0 * cfg.T * cfg.H * cfg.E
+    hbm_gbs, _, peak_src = peaks()
+    achieved = nbytes / (ms / 1000.0) / 1e9
+    line = {"metric": "router tokens/sec on 1 GB300", "value": world * cfg.T / (ms / 1000.0),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in, fp32 sums", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "part": "router (logits, top-k, softmax)",
+                       "l2_flush": "256 MiB write before every step",
+                       "graph": "one CUDA graph per step", "launches_per_step": 2,
+                       "flops_per_step": flops},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "peak_source": peak_src,
+                         "algorithmic_bytes_per_step": nbytes}}
+    print(json.dumps(line), flush=True)
+
+
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "quant.cuh", "internal.h")
 
 
@@ -306,19 +357,32 @@ def main():
     cfg = syn.CONFIGS[args.config]
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.part == "router":
+        run_router(args, nb, syn, cfg, dev, world, torch)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
 
     # ---- inputs (resident in HBM) ----
-    q1s, s1s, g1s, q2s, s2s, g2s = [], [], [], [], [], []
+    q1s, s1s, g1s, q2s, s2s, g2s, gus = [], [], [], [], [], [], []
+    split = args.gate_up_scales == "split"
     for e in range(cfg.E):
         w1 = syn.draw_weight(cfg, 1, e, device=dev)[None]
         w2 = syn.draw_weight(cfg, 2, e, device=dev)[None]
-        q, s, g = nb.quantize_weights(w1)
-        q1s.append(q); s1s.append(s); g1s.append(g)
+        if split:
+            qg, sg, gg = nb.quantize_weights(w1[:, :, :cfg.I].contiguous())
+            qu, su, gu = nb.quantize_weights(w1[:, :, cfg.I:].contiguous())
+            q1s.append(torch.cat([qg, qu], 2)); s1s.append(torch.cat([sg, su], 2))
+            g1s.append(gg); gus.append(gu)
+        else:
+            q, s, g = nb.quantize_weights(w1)
+            q1s.append(q); s1s.append(s); g1s.append(g)
         q, s, g = nb.quantize_weights(w2)
         q2s.append(q); s2s.append(s); g2s.append(g)
         del w1, w2
     pw = nb.PreparedWeights.from_checkpoint(torch.cat(q1s), torch.cat(s1s), torch.cat(g1s),
-                                            torch.cat(q2s), torch.cat(s2s), torch.cat(g2s))
+                                            torch.cat(q2s), torch.cat(s2s), torch.cat(g2s),
+                                            gs1_up=torch.cat(gus) if split else None)
     del q1s, s1s, q2s, s2s
     x_h = syn.draw_activations(cfg).pin_memory()
     ids_h, w_h = syn.draw_routing(cfg)
@@ -489,6 +553,7 @@ def main():
                        "graph": "one CUDA graph per step", "active_experts": E_act,
                        "api": "moe_nvfp4_layer_forward" if args.api == "layer"
                               else "route + quantise + forward + reduce",
+                       "gate_up_scales": args.gate_up_scales,
                        "algorithmic_bytes_per_step": step_bytes, "flops_per_step": flops,
                        "step_hbm_frac": (step_bytes / (ms_per_step / 1000.0) / 1e9) / hbm_gbs,
                        "stage_ms": {k: statistics.mean(v) for k, v in stage.items()},

@@ -306,6 +306,30 @@ int moe_nvfp4_forward(const nvmoe_weights* weights, const uint8_t* xq,
                       float* slot_out, const nvmoe_taps* taps,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* -------------------------------------------------------- router front end --
+ * moe_router_topk — the step before the routing permutation.  The pages keep
+ * the router ("gate") weight in BF16 ("NVFP4 MegaMoE Debug Log", Checkpoint
+ * Layers) and route each token to its top-k experts with softmax weights:
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h]   (bf16 inputs, fp32 sums;
+ *                  the h order is fixed, so results do not depend on timing)
+ *   topk_ids[t, j]  the expert with the j-th largest logit (ties: the lower
+ *                   expert id first)
+ *   topk_w[t, j]    softmax_mode NVMOE_ROUTER_SELECTED: softmax over the k
+ *                   selected logits; NVMOE_ROUTER_ALL: the full softmax's
+ *                   probability of the selected expert
+ *   x bf16 [T, H];  w_router bf16 [E, H];  topk_ids int32 [T, k];
+ *   topk_w float [T, k]
+ * Workspace: moe_router_workspace_size(T, H, E) bytes (no zero-fill needed).
+ * Limits: H % 128 == 0, 1 <= E <= 256, 1 <= k <= min(E, 32); x and w_router
+ * 16-byte aligned.
+ */
+#define NVMOE_ROUTER_SELECTED 0
+#define NVMOE_ROUTER_ALL 1
+size_t moe_router_workspace_size(int64_t T, int H, int E);
+int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E, int k,
+                    int softmax_mode, int32_t* topk_ids, float* topk_w, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- step 7 --
  * moe_unpermute_reduce — "scatter with routing weights" of the NVFP4 MoE
  * Pipeline, written as a deterministic gather:

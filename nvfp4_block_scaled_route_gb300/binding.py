@@ -70,6 +70,8 @@ SIGNATURES = {
     "moe_nvfp4_forward": (_I, [ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _I64, _I, _P,
                                ctypes.POINTER(Taps), _P, _SZ, _P]),
     "moe_unpermute_reduce": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _I, _P]),
+    "moe_router_workspace_size": (_SZ, [_I64, _I, _I]),
+    "moe_router_topk": (_I, [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_nvfp4_layer_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_nvfp4_layer_forward": (_I, [ctypes.POINTER(Weights), _P, _I, _P, _P, _I64, _I, _P, _I,
                                      ctypes.POINTER(Taps), _P, _SZ, _P]),
@@ -247,6 +249,26 @@ class PreparedWeights:
         if self.gs_w1_up is not None:
             ts.append(self.gs_w1_up)
         return sum(t.numel() * t.element_size() for t in ts)
+
+
+# -------------------------------------------------------- router front end --
+ROUTER_SELECTED, ROUTER_ALL = 0, 1
+
+
+def router_topk(x: torch.Tensor, w_router: torch.Tensor, k: int, mode: int = ROUTER_SELECTED,
+                ws: Optional[torch.Tensor] = None, stream=None):
+    """bf16 x [T, H], bf16 w_router [E, H] -> (topk_ids int32 [T, k], topk_w float [T, k])."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = _workspace(lib().moe_router_workspace_size(T, H, E), dev)
+    _check("moe_router_topk", lib().moe_router_topk(
+        _ptr(x), _ptr(w_router), T, H, E, k, mode, _ptr(ids), _ptr(w), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return ids, w
 
 
 # ------------------------------------------------------------- steps 3-6 --

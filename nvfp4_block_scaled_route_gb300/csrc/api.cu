@@ -452,6 +452,31 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   return NVMOE_OK;
 }
 
+// ------------------------------------------------------------ router ----
+size_t moe_router_workspace_size(int64_t T, int H, int E) {
+  if (T < 0 || H < 1 || E < 1) return 0;
+  return router_workspace_bytes(T, H, E);
+}
+
+int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E, int k,
+                    int softmax_mode, int32_t* topk_ids, float* topk_w, void* ws,
+                    size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || H < 1 || E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopK || k > E)
+    return NVMOE_ERR_INVALID_ARG;
+  if (softmax_mode != NVMOE_ROUTER_SELECTED && softmax_mode != NVMOE_ROUTER_ALL)
+    return NVMOE_ERR_INVALID_ARG;
+  if (H % 128 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return NVMOE_OK;
+  if (x == nullptr || w_router == nullptr || topk_ids == nullptr || topk_w == nullptr ||
+      ws == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(ws)) return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < moe_router_workspace_size(T, H, E)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  return status_of(counted(launch_router(x, w_router, T, H, E, k, softmax_mode, topk_ids,
+                                         topk_w, static_cast<float*>(ws), stream),
+                           2));
+}
+
 // ------------------------------------------------------------ reduce ----
 int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of, const float* topk_w,
                          int64_t T, int k, int64_t H, void* y, int y_dtype,

@@ -133,6 +133,12 @@ cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps
                              cudaStream_t stream);
 
 // ---- reduce ----
+// Router front-end (router.cu): logits partials [splits][T][E] fp32 in the
+// workspace, then top-k and softmax per token.
+size_t router_workspace_bytes(int64_t T, int H, int E);
+cudaError_t launch_router(const void* x, const void* w, int64_t T, int H, int E, int k, int mode,
+                          int32_t* ids, float* weights, float* partials, cudaStream_t stream);
+
 cudaError_t launch_reduce(const float* slot_out, const int32_t* slot_of, const float* topk_w,
                           int64_t T, int k, int64_t H, void* y, int y_dtype,
                           cudaStream_t stream);

@@ -108,6 +108,15 @@ def draw_weight(cfg: MoEConfig, layer: int, e: int, device="cpu") -> torch.Tenso
     return w.mul_(cfg.w_std * u)
 
 
+def draw_router_weight(cfg: MoEConfig, device="cpu") -> torch.Tensor:
+    """bf16 router weight [E, H] ~ N(0, s^2) with s = 1 / (act_std * sqrt(H)),
+    so that the logits of the workload's activations are about N(0, 1), the
+    distribution the routing recipes draw them from."""
+    g = _gen(device, cfg.seed, "router", cfg.E, cfg.H)
+    w = torch.randn((cfg.E, cfg.H), generator=g, device=device, dtype=torch.float32)
+    return w.mul_(1.0 / (cfg.act_std * math.sqrt(cfg.H))).to(torch.bfloat16)
+
+
 def draw_activations(cfg: MoEConfig, device="cpu", T: Optional[int] = None) -> torch.Tensor:
     """bf16 activations x[T, H] (fp32 draw, rounded to bf16 nearest-even)."""
     T = cfg.T if T is None else T
