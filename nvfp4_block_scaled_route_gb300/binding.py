@@ -401,5 +401,43 @@ class FusedLayer:
             self.ws.numel(), _stream(stream)))
         return self.y
 
+    def staging(self, x_dtype=torch.bfloat16):
+        """Pinned host buffers for a step's inputs (x, topk_ids, topk_w) in one
+        allocation, with a device twin of the same layout, and a pinned host
+        y: a step then moves its inputs in one host-to-device copy and y in
+        one device-to-host copy (forward_staged).  Returns the host views
+        (x, topk_ids, topk_w, y) to fill and read, and the device views
+        (x, topk_ids, topk_w) that forward_staged passes to the layer."""
+        T, k, H = self.T, self.k, self.w.H
+        el = torch.tensor([], dtype=x_dtype).element_size()
+        parts = [T * H * el, T * k * 4, T * k * 4]
+        offs, o = [], 0
+        for n in parts:
+            offs.append(o)
+            o += (n + 255) // 256 * 256
+        dev = self.y.device
+        host = torch.empty(max(o, 256), dtype=torch.uint8).pin_memory()
+        devb = torch.empty(max(o, 256), dtype=torch.uint8, device=dev)
+
+        def views(buf):
+            return (buf[offs[0]:offs[0] + parts[0]].view(x_dtype).view(T, H),
+                    buf[offs[1]:offs[1] + parts[1]].view(torch.int32).view(T, k),
+                    buf[offs[2]:offs[2] + parts[2]].view(torch.float32).view(T, k))
+        y_host = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+        self._stage = (host, devb, views(devb), y_host)
+        return views(host) + (y_host,), views(devb)
+
+    def forward_staged(self, stream=None, taps: Optional[dict] = None) -> torch.Tensor:
+        """One step from the pinned staging buffers (staging()): inputs to the
+        device in one copy, the layer, y back in one copy; all on `stream`.
+        Returns the pinned host y (valid once the stream has reached it)."""
+        host, devb, (x, ids, w), y_host = self._stage
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            devb.copy_(host, non_blocking=True)
+            self.forward(x, ids, w, taps=taps, stream=s)
+            y_host.copy_(self.y, non_blocking=True)
+        return y_host
+
     def status(self) -> int:
         return read_status(self.ws)

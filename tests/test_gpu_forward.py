@@ -415,3 +415,27 @@ def test_forward_gate_up_scales(nb, name, path):
     if sum(flips):
         _, y64 = flip_adjusted(ref, hq_g, hsf_g, w2q, w.numpy())
     rows_close(y.cpu().numpy(), y64, "y")
+
+
+def test_layer_staged_host_step(nb):
+    """forward_staged: inputs from the pinned staging area in one copy, y
+    back in one copy; the same bits as forward() on device tensors."""
+    cfg = syn.CONFIGS["decode1"]
+    x = syn.draw_activations(cfg)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e, device=DEV) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e, device=DEV) for e in range(cfg.E)])
+    q1, s1, g1 = nb.quantize_weights(W1)
+    q2, s2, g2 = nb.quantize_weights(W2)
+    del W1, W2
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    layer = nb.FusedLayer(pw, cfg.T, cfg.k, device=DEV)
+    y_dev = layer.forward(x.to(DEV), ids.to(DEV), w.to(DEV)).cpu()
+    (hx, hids, hw, hy), _ = layer.staging()
+    hx.copy_(x)
+    hids.copy_(ids)
+    hw.copy_(w)
+    out = layer.forward_staged()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(out, y_dev)
