@@ -528,13 +528,16 @@ def main():
         y_h = torch.empty((cfg.T, H), dtype=torch.bfloat16).pin_memory()
 
         if staged is not None:
+            # the whole staged step (inputs in, the layer, y out) as one graph:
+            # every step still copies its inputs and its output
             y_h = staged[3]
-            host_buf, dev_buf = layer._stage[0], layer._stage[1]
+            e2e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graph, stream=stream):
+                layer.forward_staged(stream=stream)
+            stream.synchronize()
 
             def e2e_step():
-                dev_buf.copy_(host_buf, non_blocking=True)
-                graph.replay()
-                y_h.copy_(layer.y, non_blocking=True)
+                e2e_graph.replay()
         else:
             def e2e_step():
                 x.copy_(x_h, non_blocking=True)
