@@ -352,17 +352,23 @@ int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of,
  *   y        [T, H] of y_dtype
  * Small batches (bf16 x, T*k <= 128, T*H <= 65536, fewer than 4 tiles per SM
  * in both GEMMs) run as ONE cooperative kernel: every CTA builds the routing
- * tables and quantises the activation rows of its own tiles, so weight
- * streaming starts at once; a single grid barrier separates L1 from the
- * requantisation (the intermediate global scale needs every h); the top-k
- * reduce of a (token, 256-column tile) is done by the CTA that writes its
- * last slot row.  taps->path = NVMOE_PATH_LAYER forces that kernel
+ * tables and computes gs_x itself, so weight streaming starts at once; the
+ * activation blocks are quantised once, 1/G of them per CTA, and each CTA's
+ * activation loads wait for the count of finished shares; a single grid
+ * barrier separates L1 from the requantisation (the intermediate global
+ * scale needs every h), which is spread over the grid the same way; the
+ * top-k reduce of a (token, 256-column tile) is done by the CTA that writes
+ * its last slot row.  taps->path = NVMOE_PATH_LAYER forces that kernel
  * (NVMOE_ERR_UNSUPPORTED_SHAPE when the batch is too large); SEPARATE / FUSED
  * select the paths of moe_nvfp4_forward after separate routing and
  * quantisation launches.  taps->slot_of, when given, receives the slot row
  * of every (token, choice).
  * Workspace: moe_nvfp4_layer_workspace_size bytes, zero-filled before first
- * use; its status word (nvmoe_read_status) is the forward's.
+ * use; its status word (nvmoe_read_status) is the forward's.  The kernel
+ * leaves its barrier words and reduce counters at zero for the next call;
+ * after a call that recorded a non-zero status (an expert id outside
+ * [0, E), a timed-out wait) they may be left mid-count: zero the workspace
+ * again before reusing it.
  */
 size_t moe_nvfp4_layer_workspace_size(int64_t T, int k, int E, int H, int I);
 int moe_nvfp4_layer_forward(const nvmoe_weights* weights, const void* x, int x_dtype,
