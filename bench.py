@@ -63,6 +63,9 @@ def parse():
                    help="one-call layer entry point, or route/quantise/forward/reduce")
     p.add_argument("--gate-up-scales", choices=["joint", "split"], default="joint",
                    help="one L1 weight global scale per expert, or separate gate/up scales")
+    p.add_argument("--mid-scale", choices=["dynamic", "static"], default="dynamic",
+                   help="the pages' dynamic intermediate scale, or a static per-expert one "
+                        "(calibrated as one dynamic forward's scale)")
     p.add_argument("--part", choices=["layer", "router"], default="layer",
                    help="the MoE layer (steps 1-7), or the router front-end alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -388,6 +391,14 @@ def main():
     ids_h, w_h = syn.draw_routing(cfg)
     ids_h, w_h = ids_h.pin_memory(), w_h.pin_memory()
     Layer = nb.FusedLayer if args.api == "layer" else nb.MoELayer
+    if args.mid_scale == "static":
+        # calibration: one dynamic forward gives the static scale of every expert
+        cal = Layer(pw, cfg.T, cfg.k, device=dev, out_dtype=torch.bfloat16)
+        gs_h = torch.zeros(1, dtype=torch.float32, device=dev)
+        cal.forward(x_h.to(dev), ids_h.to(dev), w_h.to(dev), taps={"gs_h": gs_h})
+        torch.cuda.synchronize()
+        pw.gs_mid = gs_h.expand(cfg.E).contiguous()
+        del cal
     layer = Layer(pw, cfg.T, cfg.k, device=dev, out_dtype=torch.bfloat16)
     staged = None
     if args.api == "layer":
@@ -579,6 +590,7 @@ def main():
                        "api": "moe_nvfp4_layer_forward" if args.api == "layer"
                               else "route + quantise + forward + reduce",
                        "gate_up_scales": args.gate_up_scales,
+                       "mid_scale": args.mid_scale,
                        "algorithmic_bytes_per_step": step_bytes, "flops_per_step": flops,
                        "step_hbm_frac": (step_bytes / (ms_per_step / 1000.0) / 1e9) / hbm_gbs,
                        "stage_ms": {k: statistics.mean(v) for k, v in stage.items()},

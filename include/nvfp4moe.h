@@ -230,6 +230,13 @@ int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt,
  *          equivalent to a per-column alpha).  When given, the gate columns
  *          use alpha = gs_x * gs_w1[e] and the up columns alpha = gs_x *
  *          gs_w1_up[e]; when NULL both halves use gs_w1[e].
+ *   gs_mid float [E] or NULL.  A static global scale per expert for the
+ *          requantisation of h (like a checkpoint's calibrated w2 input
+ *          scale), in place of the pages' dynamic one (amax of h over all
+ *          slots / 2688, "NVFP4 MegaMoE Debug Log", NVFP4 MoE Pipeline).
+ *          With it no step waits for the whole L1 output: each CTA
+ *          requantises the h tiles it has just produced, and L2 uses
+ *          alpha = gs_mid[e] * gs_w2[e].  taps->gs_h is not written.
  */
 typedef struct {
   int E, H, I;
@@ -240,6 +247,7 @@ typedef struct {
   const uint8_t* w2_sf;
   const float* gs_w2;
   const float* gs_w1_up;
+  const float* gs_mid;
 } nvmoe_weights;
 
 /* Optional outputs of intermediate results (any member may be NULL).

@@ -34,7 +34,7 @@ class Weights(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("w1", ctypes.c_void_p), ("w1_sf", ctypes.c_void_p), ("gs_w1", ctypes.c_void_p),
                 ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("gs_w2", ctypes.c_void_p),
-                ("gs_w1_up", ctypes.c_void_p)]
+                ("gs_w1_up", ctypes.c_void_p), ("gs_mid", ctypes.c_void_p)]
 
 
 class Taps(ctypes.Structure):
@@ -227,27 +227,33 @@ class PreparedWeights:
     w2_sf: torch.Tensor
     gs_w2: torch.Tensor
     gs_w1_up: Optional[torch.Tensor] = None
+    gs_mid: Optional[torch.Tensor] = None
 
     def struct(self) -> Weights:
         return Weights(self.E, self.H, self.I, _ptr(self.w1), _ptr(self.w1_sf), _ptr(self.gs_w1),
-                       _ptr(self.w2), _ptr(self.w2_sf), _ptr(self.gs_w2), _ptr(self.gs_w1_up))
+                       _ptr(self.w2), _ptr(self.w2_sf), _ptr(self.gs_w2), _ptr(self.gs_w1_up),
+                       _ptr(self.gs_mid))
 
     @staticmethod
-    def from_checkpoint(w1q, w1sf, gs1, w2q, w2sf, gs2, gs1_up=None) -> "PreparedWeights":
+    def from_checkpoint(w1q, w1sf, gs1, w2q, w2sf, gs2, gs1_up=None,
+                        gs_mid=None) -> "PreparedWeights":
         """w1q (E, H/2, 2I), w1sf (E, H/16, 2I), w2q (E, I/2, H), w2sf (E, I/16, H);
         gs1_up (E,) when the checkpoint quantised gate and up separately
-        (then gs1 is the gate half's scale)."""
+        (then gs1 is the gate half's scale); gs_mid (E,) a static
+        intermediate scale per expert (None: the dynamic global one)."""
         E, H2, N1 = w1q.shape
         q1, s1 = prepare_weights(w1q, w1sf)
         q2, s2 = prepare_weights(w2q, w2sf)
         return PreparedWeights(E, 2 * H2, N1 // 2, q1, s1, gs1.contiguous(), q2, s2,
                                gs2.contiguous(),
-                               gs1_up.contiguous() if gs1_up is not None else None)
+                               gs1_up.contiguous() if gs1_up is not None else None,
+                               gs_mid.contiguous() if gs_mid is not None else None)
 
     def nbytes(self) -> int:
         ts = [self.w1, self.w1_sf, self.gs_w1, self.w2, self.w2_sf, self.gs_w2]
-        if self.gs_w1_up is not None:
-            ts.append(self.gs_w1_up)
+        for t in (self.gs_w1_up, self.gs_mid):
+            if t is not None:
+                ts.append(t)
         return sum(t.numel() * t.element_size() for t in ts)
 
 

@@ -374,6 +374,11 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a1.gs_a = gs_x;
   a1.gs_b = w->gs_w1;
   a1.gs_b_up = w->gs_w1_up;
+  a1.gs_mid = w->gs_mid;
+  a1.mid_q = b.hq;
+  a1.mid_sf = b.hsf;
+  // the layer kernel requantises after its grid barrier, spread over the grid
+  a1.mid_in_epilogue = layer == nullptr;
   a1.out = b.h;
   a1.tap = tap_l1;
   a1.amax_partial = b.amax;
@@ -393,6 +398,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a2.b_sf = w->w2_sf;
   a2.gs_a = b.gs_h;
   a2.gs_b = w->gs_w2;
+  a2.gs_mid = w->gs_mid;
   a2.out = slot_out;
   a2.tap = nullptr;
   a2.amax_partial = nullptr;
@@ -441,10 +447,13 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;
   if (timed && cudaEventRecord(ev[1], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
-  // requantise h over the valid rows (global amax from the L1 partials)
-  e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1, b.hq,
-                                nullptr, b.hsf, b.gs_h, stream), 1);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (w->gs_mid == nullptr) {
+    // requantise h over the valid rows (global amax from the L1 partials);
+    // with a static intermediate scale the L1 epilogue has done it
+    e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1,
+                                  b.hq, nullptr, b.hsf, b.gs_h, stream), 1);
+    if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  }
   if (timed && cudaEventRecord(ev[2], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
   e = counted(launch_gemm(a2, map_h, map_w2, grid_for(tiles2), stream), 1);
   if (e != cudaSuccess) return NVMOE_ERR_CUDA;

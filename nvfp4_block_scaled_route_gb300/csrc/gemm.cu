@@ -616,6 +616,44 @@ __device__ void y_after_tile(const YReduce& yr, const TileInfo& ti, const Tables
   epi_bar();
 }
 
+// With a static intermediate scale: requantise the 128 h columns of a
+// finished L1 tile (its valid rows) with gs_mid[e], by the CTA that wrote
+// them (epilogue warps; the h stores are visible to the CTA after the
+// barrier).  One thread per 4-block quad, so a staged 32-bit scale word is
+// written whole; the same block arithmetic as every other quantisation.
+__device__ void requant_own_tile(const GemmArgs& args, const TileInfo& ti, const Tables& tb) {
+  epi_bar();
+  const float gs = __ldg(args.gs_mid + ti.e);
+  const float denom = __fmul_rn(6.0f, gs);
+  const int I = args.I;
+  const int k_atoms = (I + kStageK - 1) / kStageK * 4;
+  const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
+  const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
+  const int g_base = ti.nt * 8;                       // 128 columns = 8 blocks
+  for (int u = threadIdx.x - 64; u < n_valid * 2; u += 128) {
+    const int64_t row = row0 + (u >> 1);
+    const int g0 = g_base + (u & 1) * 4;
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float4* p = reinterpret_cast<const float4*>(args.out + row * I + (g0 + b) * 16);
+      float v[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 f = __ldcg(p + c);
+        v[4 * c] = f.x; v[4 * c + 1] = f.y; v[4 * c + 2] = f.z; v[4 * c + 3] = f.w;
+      }
+      uint32_t packed[2];
+      word |= quant_block16(v, gs, denom, packed) << (8 * b);
+      *reinterpret_cast<uint2*>(args.mid_q + row * (I / 2) + (g0 + b) * 8) =
+          make_uint2(packed[0], packed[1]);
+    }
+    *reinterpret_cast<uint32_t*>(args.mid_sf + staged_offset(row, g0, k_atoms)) = word;
+  }
+  // the L2 activation loads (async proxy) come after a grid-wide sync
+  fence_proxy_async_global();
+}
+
 // Four warps (128 threads, one accumulator row each).  Returns false when
 // a wait gave up; the decision is shared so all four warps leave together.
 // gs_a is the activations' global scale, passed by value: the caller knows
@@ -636,19 +674,23 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
   // the weight scales of the next tile are loaded one tile ahead; the up
   // half of L1 has its own scale when the checkpoint gives one
   const float* gs_b_up = args.gs_b_up != nullptr ? args.gs_b_up : args.gs_b;
+  // L2 with a static intermediate scale: the activation scale is per expert
+  const bool mid_alpha = args.mode == 2 && args.gs_mid != nullptr;
   int e0 = have ? decode_tile(tile, P.prefix, tb.mtiles, E).e : 0;
   float gs_b = have ? __ldg(args.gs_b + e0) : 0.0f;
   float gs_u = have ? __ldg(gs_b_up + e0) : 0.0f;
+  float gs_m = have && mid_alpha ? __ldg(args.gs_mid + e0) : gs_a;
   while (have) {
     const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
-    const float alpha = __fmul_rn(gs_a, gs_b);
-    const float alpha_u = __fmul_rn(gs_a, gs_u);
+    const float alpha = __fmul_rn(gs_m, gs_b);
+    const float alpha_u = __fmul_rn(gs_m, gs_u);
     int n_tile, n_s0, n_s1;
     const bool n_have = it.next(n_tile, n_s0, n_s1);
     if (n_have) {
       const int ne = decode_tile(n_tile, P.prefix, tb.mtiles, E).e;
       gs_b = __ldg(args.gs_b + ne);
       gs_u = __ldg(gs_b_up + ne);
+      if (mid_alpha) gs_m = __ldg(args.gs_mid + ne);
     }
     // one thread waits (bounded) and the decision is shared, so the four
     // epilogue warps always take the same path through the named barriers
@@ -694,6 +736,8 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->acc_empty);
       if (yr != nullptr) y_after_tile(*yr, ti, tb, args);
+      if (args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue)
+        requant_own_tile(args, ti, tb);
     } else {
       // a piece of a split tile: park the raw accumulator in the workspace
       float* mine = args.partials +
@@ -758,6 +802,8 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
             epi_l2_4(a, alpha, row0 + r, col0 + g4 * 4, args);
         }
         if (yr != nullptr) y_after_tile(*yr, ti, tb, args);
+        if (args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue)
+          requant_own_tile(args, ti, tb);
       }
     }
     pp.acc_phase ^= 1u;
@@ -980,6 +1026,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
     bool ok = run_epilogue(P1, __ldcg(a1.gs_a), E, tb, bars, tmem, pp, abort, amax, &s_ok,
                            &s_last);
     publish_amax(amax, s_amax, a1.amax_partial);
+    if (a1.gs_mid != nullptr) {
+      // static intermediate scale: every tile was requantised by its own CTA;
+      // one barrier (generation 2 opens the producer's L2 activation loads)
+      if (warp == 2 && lane == 0)
+        s_ok = ok && grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
+      epi_bar();
+      ok = s_ok != 0;
+    } else {
     // barrier 1: every h row and every per-CTA amax is written
     if (warp == 2 && lane == 0)
       s_ok = ok && grid_barrier(f.grid_bar, 1, a1.status, abort) ? 1 : 0;
@@ -995,6 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
       if (warp == 2 && lane == 0) s_ok = grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
       epi_bar();
       ok = s_ok != 0;
+    }
     }
     // gs_h is final: the requantisation before the second barrier wrote it
     if (ok)
@@ -1053,10 +1108,10 @@ struct LayerArgs {
 // bytes of a staged 32-bit word come from 4 neighbouring lanes.
 template <bool kFromTokens>
 __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
-                               const int* slot_row, uint8_t* q, uint8_t* sf, float gs) {
+                               const int* slot_row, uint8_t* q, uint8_t* sf, float gs_all,
+                               const float* gs_expert = nullptr, const int32_t* ids = nullptr) {
   const int bpr = cols >> 4;
   const int k_atoms = (cols + kStageK - 1) / kStageK * 4;
-  const float denom = __fmul_rn(6.0f, gs);
   const int etid = threadIdx.x - 64;
   const int n_quads = n_rows * (bpr >> 2);
   const int q0 = static_cast<int>(static_cast<int64_t>(n_quads) * blockIdx.x / gridDim.x);
@@ -1069,6 +1124,7 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
     const int g = active ? b - r * bpr : 0;
     float v[16];
     int row = -1;
+    float gs = gs_all;
     if (kFromTokens) {
       uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
       if (active) {
@@ -1085,6 +1141,9 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
       }
     } else {
       if (active) row = slot_row[r];
+      // h rows (flat slot r) under a static per-expert intermediate scale
+      // (a slot with no row, i.e. an invalid expert id, is skipped)
+      if (gs_expert != nullptr && row >= 0) gs = __ldg(gs_expert + ids[r]);
       float4 f[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1103,7 +1162,7 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
       }
     }
     uint32_t packed[2];
-    const uint32_t s = quant_block16(v, gs, denom, packed);
+    const uint32_t s = quant_block16(v, gs, __fmul_rn(6.0f, gs), packed);
     const uint32_t word = s | (__shfl_down_sync(0xFFFFFFFFu, s, 1) << 8) |
                           (__shfl_down_sync(0xFFFFFFFFu, s, 2) << 16) |
                           (__shfl_down_sync(0xFFFFFFFFu, s, 3) << 24);
@@ -1316,7 +1375,15 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     }
     epi_bar();
     ok = s_ok != 0;
-    if (ok) {
+    if (ok && a1.gs_mid != nullptr) {
+      // static intermediate scale: no global max; the share of h is
+      // requantised with the scale of each slot's expert
+      quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, 0.0f, a1.gs_mid, L.topk_ids);
+      share_done(&L.grid_bar[4]);
+      YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
+                 s_scratch, &s_n};
+      run_epilogue(P2, 0.0f, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
+    } else if (ok) {
       const float gs = global_scale_from(__int_as_float(ld_acquire(&L.grid_bar[5])));
       if (blockIdx.x == 0 && lead) *L.gs_h = gs;
       quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, gs);

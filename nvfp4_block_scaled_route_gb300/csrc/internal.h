@@ -74,6 +74,14 @@ struct GemmArgs {
   const float* gs_a;      // [1]
   const float* gs_b;      // [E]
   const float* gs_b_up;   // L1: [E] scale of the up half, or null (= gs_b)
+  const float* gs_mid;    // [E] static intermediate scale, or null (dynamic).  L1:
+                          // each finished tile of h is requantised with
+                          // gs_mid[e] into mid_q / mid_sf by its own CTA;
+                          // L2: alpha = gs_mid[e] * gs_b[e] (gs_a unused)
+  uint8_t* mid_q;         // L1 with gs_mid: hq [rows, I/2]
+  uint8_t* mid_sf;        // L1 with gs_mid: staged scales of hq
+  bool mid_in_epilogue;   // L1 with gs_mid: requantise in the epilogue (else the
+                          // caller requantises after its grid barrier)
   float* out;             // L1: h [rows, I]; L2: slot_out [rows, N]
   float* tap;             // L1: l1_out [rows, 2I] or null
   float* amax_partial;    // L1: [grid]

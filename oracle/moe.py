@@ -176,12 +176,15 @@ def quantize_expert_weights(w_list, split_halves: bool = False):
 
 
 def forward(x, topk_ids, topk_w, w1_q, w1_sf, gs_w1, w2_q, w2_sf, gs_w2,
-            expert_subset=None):
+            expert_subset=None, gs_mid=None):
     """Whole forward pass.  x: [T, H] float32 holding bf16 values.
 
     Weights in checkpoint layout: w1_q (E, H/2, 2I), w1_sf (E, H/16, 2I),
     w2_q (E, I/2, H), w2_sf (E, I/16, H), gs_w* (E,); gs_w1 may be (E, 2)
-    (separate gate and up global scales).  w*_q may also be a
+    (separate gate and up global scales).
+    gs_mid (E,): a static intermediate global scale per expert in place of
+    the pipeline's dynamic one: h rows of expert e are requantised with
+    gs_mid[e] and L2 takes alpha = gs_mid[e] * gs_w2[e]; gs_h is then None.  w*_q may also be a
     callable e -> (q, sf) that yields one expert at a time (to bound memory).
     Returns a dict of every intermediate (dense slot order).
     """
@@ -216,17 +219,28 @@ def forward(x, topk_ids, topk_w, w1_q, w1_sf, gs_w1, w2_q, w2_sf, gs_w2,
         I = (w1(0)[0].shape[-1]) // 2
         l1 = np.zeros((0, 2 * I))
     h = swiglu(l1)                                                # step 4
-    hq, hsf, gs_h = nvfp4.quantize_rows(h)                        # step 4
+    if gs_mid is None:
+        hq, hsf, gs_h = nvfp4.quantize_rows(h)                    # step 4
+    else:
+        hq = np.zeros((S, h.shape[1] // 2), dtype=np.uint8)
+        hsf = np.zeros((S, h.shape[1] // 16), dtype=np.uint8)
+        gs_h = None
+        for e in range(E):
+            s0, s1 = r["offsets"][e], r["offsets"][e + 1]
+            if s1 > s0:
+                hq[s0:s1], hsf[s0:s1], _ = nvfp4.quantize_rows(h[s0:s1], np.float32(gs_mid[e]))
     out2 = np.zeros((S, H), dtype=np.float64)
     for e in range(E):                                            # step 5 + 6
         s0, s1 = r["offsets"][e], r["offsets"][e + 1]
         if s1 == s0:
             continue
         q, sf = w2(e)
-        out2[s0:s1] = expert_l2(hq[s0:s1], hsf[s0:s1], gs_h, q, sf, gs_w2[e])
+        g = gs_h if gs_mid is None else np.float32(gs_mid[e])
+        out2[s0:s1] = expert_l2(hq[s0:s1], hsf[s0:s1], g, q, sf, gs_w2[e])
     y64 = unpermute_reduce(out2, r["slot_of"], topk_w)            # step 7
     return dict(route=r, xq=xq, xsf=xsf, gs_x=gs_x, l1=l1, h=h, hq=hq, hsf=hsf,
-                gs_h=gs_h, out2=out2, y64=y64, y_bf16=nvfp4.round_to_bf16(y64))
+                gs_h=gs_h, gs_mid=gs_mid, out2=out2, y64=y64,
+                y_bf16=nvfp4.round_to_bf16(y64))
 
 
 def cosine(a, b) -> float:

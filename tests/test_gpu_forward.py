@@ -72,12 +72,14 @@ def e4m3_boundaries():
 
 def check_requant(h_or, gs_or, hq_or, hsf_or, hq_gpu, hsf_gpu):
     """Flips of the requantised intermediate must sit on rounding boundaries
-    of the oracle's own values.  Returns (scale flips, nibble flips)."""
+    of the oracle's own values.  gs_or: one scale, or one per row.  Returns
+    (scale flips, nibble flips)."""
     S, I = h_or.shape
     blocks = h_or.reshape(S, I // 16, 16).astype(np.float64)
+    gs_rows = np.broadcast_to(np.asarray(gs_or, np.float64).reshape(-1, 1), (S, 1))
     sf_flip = hsf_gpu != hsf_or
     if sf_flip.any():
-        t = np.abs(blocks).max(-1) / (6.0 * float(gs_or))
+        t = np.abs(blocks).max(-1) / (6.0 * gs_rows)
         assert near_boundary(t[sf_flip], e4m3_boundaries()).all(), "scale flip off a boundary"
     nib_g = onv.unpack_nibbles(hq_gpu).reshape(S, I // 16, 16)
     nib_o = onv.unpack_nibbles(hq_or).reshape(S, I // 16, 16)
@@ -87,7 +89,7 @@ def check_requant(h_or, gs_or, hq_or, hsf_or, hq_gpu, hsf_gpu):
     same_zero = ((nib_g & 7) == 0) & ((nib_o & 7) == 0)
     diff &= ~same_zero
     if diff.any():
-        d = onv.e4m3_decode(hsf_or).astype(np.float64) * float(gs_or)
+        d = onv.e4m3_decode(hsf_or).astype(np.float64) * gs_rows
         r = np.abs(blocks) / d[..., None]
         assert near_boundary(r[diff], E2M1_BOUNDARIES).all(), "nibble flip off a boundary"
     return int(sf_flip.sum()), int(diff.sum())
@@ -106,9 +108,9 @@ def flip_adjusted(ref, hq_g, hsf_g, w2, topk_w):
     diff = deq_g - deq_or
     out2 = np.array(ref["out2"], dtype=np.float64, copy=True)
     offsets = np.asarray(ref["route"]["offsets"])
-    gs_h = float(ref["gs_h"])
     for s_ in np.nonzero(np.any(diff != 0, axis=1))[0]:
         e = int(np.searchsorted(offsets, s_, side="right") - 1)
+        gs_h = float(ref["gs_h"]) if ref.get("gs_mid") is None else float(ref["gs_mid"][e])
         W = onv.dequantize_weight(w2q[e], w2sf[e])
         out2[s_] += (diff[s_] @ W) * (gs_h * float(gs_w2[e]))
     y64 = omoe.unpermute_reduce(out2, ref["route"]["slot_of"], topk_w)
@@ -439,3 +441,52 @@ def test_layer_staged_host_step(nb):
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert torch.equal(out, y_dev)
+
+
+
+# ------------------------------------------ static intermediate scale ----
+
+@pytest.mark.parametrize("name,path", [("tiny", 1), ("tiny", 2), ("tiny", 3),
+                                       ("small", 1), ("small", 2), ("medium", 1)])
+def test_forward_static_mid_scale(nb, name, path):
+    """A static intermediate scale per expert: each CTA requantises its own
+    L1 tiles with gs_mid[e] (no global amax, no requantisation pass); L2
+    alpha gs_mid[e]*gs_w2[e].  Scales span saturating and coarse cases."""
+    cfg = syn.CONFIGS[name]
+    x = syn.draw_activations(cfg)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)])
+    w1q = omoe.quantize_expert_weights(list(W1.numpy()))
+    w2q = omoe.quantize_expert_weights(list(W2.numpy()))
+    dyn = omoe.forward(x.float().numpy(), ids.numpy(), w.numpy(), *w1q, *w2q)
+    mid = (float(dyn["gs_h"]) * np.linspace(0.3, 2.0, cfg.E)).astype(np.float32)
+    ref = omoe.forward(x.float().numpy(), ids.numpy(), w.numpy(), *w1q, *w2q, gs_mid=mid)
+    q1, s1, g1 = nb.quantize_weights(W1.to(DEV))
+    q2, s2, g2 = nb.quantize_weights(W2.to(DEV))
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2,
+                                            gs_mid=torch.from_numpy(mid).to(DEV))
+    Layer = nb.FusedLayer if path == 3 else nb.MoELayer
+    layer = Layer(pw, cfg.T, cfg.k, device=DEV, out_dtype=torch.float32)
+    rows = layer.rows
+    taps = dict(h=torch.zeros((rows, cfg.I), dtype=torch.float32, device=DEV),
+                hq=torch.zeros((rows, cfg.I // 2), dtype=torch.uint8, device=DEV),
+                hsf_mma=torch.zeros(nb.sf_mma_bytes(rows, cfg.I), dtype=torch.uint8, device=DEV),
+                slot_of=torch.zeros(cfg.T * cfg.k, dtype=torch.int32, device=DEV), path=path)
+    y = layer.forward(x.to(DEV), ids.to(DEV), w.to(DEV), taps=taps)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    row_of = taps["slot_of"].cpu().numpy() if path == 3 else \
+        layer.route.slot_of.cpu().numpy()[:cfg.T * cfg.k]
+    r = ref["route"]
+    dense_rows = np.empty(cfg.T * cfg.k, dtype=np.int64)
+    dense_rows[r["slot_of"]] = row_of
+    rows_close(taps["h"].cpu().numpy()[dense_rows], ref["h"], "h")
+    hq_g = taps["hq"].cpu().numpy()[dense_rows]
+    hsf_g = unstage(taps["hsf_mma"].cpu().numpy(), rows, cfg.I)[dense_rows]
+    slot_expert = np.searchsorted(np.asarray(r["offsets"]), np.arange(cfg.T * cfg.k), side="right") - 1
+    flips = check_requant(ref["h"], mid[slot_expert], ref["hq"], ref["hsf"], hq_g, hsf_g)
+    y64 = ref["y64"]
+    if sum(flips):
+        _, y64 = flip_adjusted(ref, hq_g, hsf_g, w2q, w.numpy())
+    rows_close(y.cpu().numpy(), y64, "y")

@@ -602,3 +602,31 @@ def test_forward_tiny_matches_brute_force():
             float(gsh) * float(g2[e]))
         y[t] += float(w[t, j]) * o
     assert np.allclose(out["y64"], y, rtol=1e-12, atol=1e-12)
+
+
+def test_static_mid_scale_equals_dynamic_when_equal():
+    """A static intermediate scale equal to the dynamic one changes nothing;
+    otherwise expert e's rows are quantised with gs_mid[e] alone."""
+    rng = np.random.default_rng(21)
+    T, k, E, H, I = 6, 2, 3, 64, 32
+    x = rng.normal(0, 1.5, (T, H)).astype(np.float32)
+    ids = np.array([rng.choice(E, k, replace=False) for _ in range(T)], dtype=np.int32)
+    w = rng.uniform(0.1, 1, (T, k)).astype(np.float32)
+    W1 = [rng.normal(0, 0.2, (H, 2 * I)).astype(np.float32) for _ in range(E)]
+    W2 = [rng.normal(0, 0.2, (I, H)).astype(np.float32) for _ in range(E)]
+    q1 = moe.quantize_expert_weights(W1)
+    q2 = moe.quantize_expert_weights(W2)
+    dyn = moe.forward(x, ids, w, *q1, *q2)
+    same = moe.forward(x, ids, w, *q1, *q2, gs_mid=np.full(E, dyn["gs_h"], np.float32))
+    assert np.array_equal(dyn["hq"], same["hq"]) and np.array_equal(dyn["hsf"], same["hsf"])
+    assert np.array_equal(dyn["y64"], same["y64"])
+    mid = np.array([0.5, 1.0, 2.0], np.float32) * dyn["gs_h"]
+    st = moe.forward(x, ids, w, *q1, *q2, gs_mid=mid)
+    r = st["route"]
+    for e in range(E):
+        s0, s1 = r["offsets"][e], r["offsets"][e + 1]
+        if s1 > s0:
+            hq, hsf, _ = nvfp4.quantize_rows(st["h"][s0:s1], mid[e])
+            assert np.array_equal(st["hq"][s0:s1], hq) and np.array_equal(st["hsf"][s0:s1], hsf)
+            want = moe.expert_l2(hq, hsf, mid[e], q2[0][e], q2[1][e], q2[2][e])
+            assert np.array_equal(st["out2"][s0:s1], want)
