@@ -336,6 +336,23 @@ def profiled_traffic(kernel: str, config: str):
     return d.get("per_launch_bytes", {}).get(config)
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (every rank gets it); the value itself when
+    there is one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time
+    (the replicas are independent, so work grows with the rank count)."""
+    return world * tokens_per_step * steps / (ms / 1000.0)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -476,13 +493,9 @@ def main():
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * cfg.T * args.steps / (total_ms / 1000.0)
+    value = job_throughput(world, cfg.T, args.steps, total_ms)
 
     # ---- dominant kernel: L1 GEMM timed alone by library-recorded events ----
     n_prof = min(args.steps, 50)
@@ -559,12 +572,8 @@ def main():
 
         timed_loop(min(args.warmup, 5), e2e_step)
         et = timed_loop(args.steps, e2e_step)
-        e_ms = sum(et)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * cfg.T * args.steps / (e_ms / 1000.0), "unit": UNIT,
+        e_ms = max_over_ranks(sum(et), world, dev)
+        e2e = {"value": job_throughput(world, cfg.T, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": (layer._stage[0].nbytes if staged is not None
                                       else x_h.nbytes + ids_h.nbytes + w_h.nbytes),
                "d2h_bytes_per_step": y_h.nbytes, "ms_per_step": e_ms / args.steps}
