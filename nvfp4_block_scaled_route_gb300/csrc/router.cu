@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
 // and accumulates every token over them; the 128 partial sums of a logit are
 // then added in a fixed tree (warp shuffles, then the four warps in order).
 constexpr int kSmallT = 32;
+constexpr int kSms = 152;               // grid sizing target (GB300)
+constexpr int kMmaMinT = 1024;          // tensor-core logits from this many tokens
 constexpr int kSmallThreads = 128;
 
 template <int TT>
@@ -151,6 +153,122 @@ __global__ void __launch_bounds__(kSmallThreads) router_logits_small_kernel(
 #pragma unroll
     for (int q = 0; q < kSmallThreads / 32; ++q) v += red[q][t];
     logits[static_cast<int64_t>(t) * E + e] = v;
+  }
+}
+
+// Larger batches: the logits as a tensor-core contraction.  A CTA takes 128
+// tokens (8 warps x 16 rows) and a column tile of NT x 8 experts
+// (blockIdx.y), and walks H in chunks of 64 that cp.async stages into a
+// four-deep shared-memory ring (three chunks in flight while one is used);
+// each warp issues mma.sync.m16n8k16 (bf16 in, fp32 accumulate) over its 16
+// rows.  The K order is fixed, so the logits do not depend on timing.
+constexpr int kMmaRows = 128;
+constexpr int kMmaK = 64;
+constexpr int kMmaStride = kMmaK + 8;   // bf16 per staged row (+16 B: no bank conflicts)
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, bool valid) {
+  // 16 bytes global -> shared, zero-filled when !valid (src is then not read)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kMmaStages = 4;
+
+template <int NT>
+__global__ void __launch_bounds__(256) router_logits_mma_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w, int64_t T, int H,
+    int E, float* __restrict__ logits) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr int kStageElems = (kMmaRows + NT * 8) * kMmaStride;
+  __nv_bfloat16* stage_base = reinterpret_cast<__nv_bfloat16*>(smem);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kMmaRows;
+  const int e0 = blockIdx.y * NT * 8;     // first expert of this CTA's column tile
+  const int chunks = H / kMmaK;
+  // chunk c -> stage c % kMmaStages: 128 token rows then NT*8 expert rows
+  auto load = [&](int c) {
+    __nv_bfloat16* xs = stage_base + (c % kMmaStages) * kStageElems;
+    __nv_bfloat16* ws = xs + kMmaRows * kMmaStride;
+    const int kc = c * kMmaK;
+    for (int i = threadIdx.x; i < kMmaRows * (kMmaK / 8); i += 256) {
+      const int r = i / (kMmaK / 8), col = (i % (kMmaK / 8)) * 8;
+      const bool ok = t0 + r < T;
+      cp_async16(xs + r * kMmaStride + col, x + (ok ? (t0 + r) * H + kc + col : 0), ok);
+    }
+    for (int i = threadIdx.x; i < NT * 8 * (kMmaK / 8); i += 256) {
+      const int r = i / (kMmaK / 8), col = (i % (kMmaK / 8)) * 8;
+      const bool ok = e0 + r < E;
+      cp_async16(ws + r * kMmaStride + col,
+                 w + (ok ? static_cast<int64_t>(e0 + r) * H + kc + col : 0), ok);
+    }
+  };
+  float acc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[n][i] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kMmaStages - 1; ++c) {
+    if (c < chunks) load(c);
+    cp_async_commit();
+  }
+  for (int c = 0; c < chunks; ++c) {
+    cp_async_wait<kMmaStages - 2>();          // chunk c has landed (this thread's part)
+    __syncthreads();                           // ... and everyone's; stage of c-1 is free
+    if (c + kMmaStages - 1 < chunks) load(c + kMmaStages - 1);
+    cp_async_commit();
+    const __nv_bfloat16* xs = stage_base + (c % kMmaStages) * kStageElems;
+    const __nv_bfloat16* ws = xs + kMmaRows * kMmaStride;
+    const __nv_bfloat16* xw = xs + (warp * 16) * kMmaStride;
+#pragma unroll
+    for (int k16 = 0; k16 < kMmaK; k16 += 16) {
+      uint32_t a[4];
+      a[0] = *reinterpret_cast<const uint32_t*>(xw + grp * kMmaStride + k16 + 2 * tig);
+      a[1] = *reinterpret_cast<const uint32_t*>(xw + (grp + 8) * kMmaStride + k16 + 2 * tig);
+      a[2] = *reinterpret_cast<const uint32_t*>(xw + grp * kMmaStride + k16 + 8 + 2 * tig);
+      a[3] = *reinterpret_cast<const uint32_t*>(xw + (grp + 8) * kMmaStride + k16 + 8 + 2 * tig);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const __nv_bfloat16* wr = ws + (n * 8 + grp) * kMmaStride + k16 + 2 * tig;
+        uint32_t b[2];
+        b[0] = *reinterpret_cast<const uint32_t*>(wr);
+        b[1] = *reinterpret_cast<const uint32_t*>(wr + 8);
+        mma_bf16_16816(acc[n], a, b);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  // D fragment: rows grp / grp + 8 of the warp's 16, columns 2*tig, 2*tig + 1
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int e = e0 + n * 8 + 2 * tig;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t t = t0 + warp * 16 + grp + 8 * h;
+      if (t < T) {
+        if (e < E) logits[t * E + e] = acc[n][2 * h];
+        if (e + 1 < E) logits[t * E + e + 1] = acc[n][2 * h + 1];
+      }
+    }
   }
 }
 
@@ -242,9 +360,9 @@ __global__ void router_topk_kernel(const float* __restrict__ partials, int split
 }
 
 int splits_for(int64_t T, int H) {
-  if (T <= kSmallT) return 1;
+  if (T <= kSmallT || T >= kMmaMinT) return 1;
   const int64_t tiles = (T + kTokPerCta - 1) / kTokPerCta;
-  int64_t s = (2 * 152) / (tiles > 0 ? tiles : 1);
+  int64_t s = (2 * kSms) / (tiles > 0 ? tiles : 1);
   const int max_s = H / kChunkK;
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
@@ -273,6 +391,40 @@ cudaError_t launch_router(const void* x, const void* w, int64_t T, int H, int E,
     else
       router_logits_small_kernel<32><<<E, kSmallThreads, 0, stream>>>(xb, wb, t, H, E, partials);
     cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    router_topk_kernel<<<static_cast<unsigned>((T + warps - 1) / warps), warps * 32, 0, stream>>>(
+        partials, 1, T, E, k, mode, ids, weights);
+    return cudaGetLastError();
+  }
+  if (T >= kMmaMinT && H % kMmaK == 0) {
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* wb = static_cast<const __nv_bfloat16*>(w);
+    // column tile: all experts in one CTA, halved (down to 64 experts) while
+    // the grid would leave SMs idle; x tiles are then re-read from L2
+    const int nt_all = (E + 7) / 8;
+    int nt = nt_all <= 2 ? 2 : nt_all <= 4 ? 4 : nt_all <= 6 ? 6 : nt_all <= 8 ? 8
+           : nt_all <= 16 ? 16 : 32;
+    const int64_t row_tiles = (T + kMmaRows - 1) / kMmaRows;
+    while (nt > 8 && row_tiles * ((nt_all + nt - 1) / nt) < kSms) nt /= 2;
+    const size_t smem =
+        static_cast<size_t>(kMmaStages) * (kMmaRows + nt * 8) * kMmaStride * 2;
+    const dim3 grid(static_cast<unsigned>(row_tiles),
+                    static_cast<unsigned>((nt_all + nt - 1) / nt));
+    auto run = [&](auto kernel) -> cudaError_t {
+      if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+      }
+      kernel<<<grid, 256, smem, stream>>>(xb, wb, T, H, E, partials);
+      return cudaGetLastError();
+    };
+    cudaError_t err = nt == 2 ? run(router_logits_mma_kernel<2>)
+                    : nt == 4 ? run(router_logits_mma_kernel<4>)
+                    : nt == 6 ? run(router_logits_mma_kernel<6>)
+                    : nt == 8 ? run(router_logits_mma_kernel<8>)
+                    : nt == 16 ? run(router_logits_mma_kernel<16>)
+                               : run(router_logits_mma_kernel<32>);
     if (err != cudaSuccess) return err;
     router_topk_kernel<<<static_cast<unsigned>((T + warps - 1) / warps), warps * 32, 0, stream>>>(
         partials, 1, T, E, k, mode, ids, weights);

@@ -122,7 +122,8 @@ def check_router(x, w, k, mode, ids_g, w_g):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["tiny", "small", "medium", "decode1", "decode64", "prefill4k"])
+@pytest.mark.parametrize("name", ["tiny", "small", "medium", "decode1", "decode64", "prefill4k",
+                                  "prefill16k"])
 def test_router_matches_oracle(nb, name):
     cfg = syn.CONFIGS[name]
     mode = "all" if cfg.routing == "softmax_topk_probs" else "selected"
@@ -156,6 +157,27 @@ def test_router_ties_and_edges(nb):
     ids, wt = nb.router_topk(x.cuda(), w.cuda(), 32)
     torch.cuda.synchronize()
     check_router(x.float().numpy(), w.float().numpy(), 32, "selected", ids.cpu().numpy(),
+                 wt.cpu().numpy())
+    # the tensor-core logits path (>= 1024 tokens): 256 experts in four
+    # column tiles, a ragged last token tile
+    x = (torch.randn((1100, 256), generator=g)).to(torch.bfloat16)
+    ids, wt = nb.router_topk(x.cuda(), w.cuda(), 8)
+    torch.cuda.synchronize()
+    check_router(x.float().numpy(), w.float().numpy(), 8, "selected", ids.cpu().numpy(),
+                 wt.cpu().numpy())
+    # ... 200 experts (ragged last column tile), H = 128 (fewer chunks than
+    # the staging ring), probabilities over all experts
+    x = (torch.randn((1030, 128), generator=g)).to(torch.bfloat16)
+    w2 = (torch.randn((200, 128), generator=g) * 0.09).to(torch.bfloat16)
+    ids, wt = nb.router_topk(x.cuda(), w2.cuda(), 6, mode=nb.ROUTER_ALL)
+    torch.cuda.synchronize()
+    check_router(x.float().numpy(), w2.float().numpy(), 6, "all", ids.cpu().numpy(),
+                 wt.cpu().numpy())
+    # ... 12 experts (one 16-wide tile, 4 padded columns)
+    w3 = (torch.randn((12, 128), generator=g) * 0.09).to(torch.bfloat16)
+    ids, wt = nb.router_topk(x.cuda(), w3.cuda(), 2)
+    torch.cuda.synchronize()
+    check_router(x.float().numpy(), w3.float().numpy(), 2, "selected", ids.cpu().numpy(),
                  wt.cpu().numpy())
     ids, wt = nb.router_topk(torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda"),
                              w.cuda(), 4)
