@@ -1106,10 +1106,15 @@ struct LayerArgs {
 // else source row i is flat slot i, read (fp32) from and written to slot
 // row slot_row[i].  Shares are whole groups of 4 blocks, so the 4 scale
 // bytes of a staged 32-bit word come from 4 neighbouring lanes.
+// dry: one pass by a whole warp through the same arithmetic and stores on
+// dummy values (no loads; slot_row all 0, q and sf a shared-memory scratch),
+// to bring the code into the SM's instruction cache before the share itself
+// is on the critical path (not inlined, so both calls run the same code).
 template <bool kFromTokens>
-__device__ void quantise_share(const void* src, int n_rows, int cols, int k,
-                               const int* slot_row, uint8_t* q, uint8_t* sf, float gs_all,
-                               const float* gs_expert = nullptr, const int32_t* ids = nullptr) {
+__device__ __noinline__ void quantise_share(const void* src, int n_rows, int cols, int k,
+                                            const int* slot_row, uint8_t* q, uint8_t* sf,
+                                            float gs_all, const float* gs_expert = nullptr,
+                                            const int32_t* ids = nullptr, bool dry = false) {
   const int bpr = cols >> 4;
   const int k_atoms = (cols + kStageK - 1) / kStageK * 4;
   const int etid = threadIdx.x - 64;
@@ -1117,17 +1122,17 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
   const int q0 = static_cast<int>(static_cast<int64_t>(n_quads) * blockIdx.x / gridDim.x);
   const int q1 = static_cast<int>(static_cast<int64_t>(n_quads) * (blockIdx.x + 1) / gridDim.x);
   const int b_end = 4 * q1;
-  for (int b0 = 4 * q0 + (etid & ~31); b0 < b_end; b0 += 128) {      // warp-uniform
+  for (int b0 = 4 * q0 + (etid & ~31); dry || b0 < b_end; b0 += 128) {      // warp-uniform
     const int b = b0 + (etid & 31);
-    const bool active = b < b_end;
-    const int r = active ? b / bpr : 0;
-    const int g = active ? b - r * bpr : 0;
+    const bool active = dry || b < b_end;
+    const int r = active && !dry ? b / bpr : 0;
+    const int g = active && !dry ? b - r * bpr : 0;
     float v[16];
     int row = -1;
     float gs = gs_all;
     if (kFromTokens) {
       uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
-      if (active) {
+      if (active && !dry) {
         const uint4* p = reinterpret_cast<const uint4*>(
             static_cast<const __nv_bfloat16*>(src) + static_cast<int64_t>(r) * cols + g * 16);
         u0 = __ldg(p);
@@ -1147,7 +1152,7 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
       float4 f[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (row >= 0) {
+      if (row >= 0 && !dry) {
         const float4* p = reinterpret_cast<const float4*>(
             static_cast<const float*>(src) + static_cast<int64_t>(row) * cols + g * 16);
 #pragma unroll
@@ -1160,6 +1165,10 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
         v[4 * c + 2] = f[c].z;
         v[4 * c + 3] = f[c].w;
       }
+    }
+    if (dry) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 1.0f + 0.25f * j;
     }
     uint32_t packed[2];
     const uint32_t s = quant_block16(v, gs, __fmul_rn(6.0f, gs), packed);
@@ -1181,6 +1190,7 @@ __device__ void quantise_share(const void* src, int n_rows, int cols, int k,
     } else if (row >= 0) {
       put(row);
     }
+    if (dry) break;
   }
 }
 
@@ -1207,6 +1217,8 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   __shared__ int s_tok[kLayerMaxSlots];       // token of dense slot
   __shared__ int s_scratch[kMaxExperts];      // running counts, then the reduce list
   __shared__ float s_gs;
+  // dry passes of the share quantisers: slot rows (all 0), then q and sf bytes
+  __shared__ __align__(16) int s_dry[kMaxTopK + 8];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a1.E, k = L.k, S = L.T * L.k;
@@ -1218,6 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     s_scratch[e] = 0;
   }
   if (threadIdx.x == 0) s_amax[0] = 0.0f;
+  if (threadIdx.x < kMaxTopK + 8) s_dry[threadIdx.x] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < S; i += blockDim.x) {
     const int e = L.topk_ids[i];
@@ -1272,6 +1285,18 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   const Phase P1 = make_phase(a1, &map_x, &map_w1, tb.prefix1, E);
   const Phase P2 = make_phase(a2, &map_h, &map_w2, tb.prefix2, E);
   Pipe pp;
+  // Warm the instruction cache with the two share quantisers while their
+  // code is off the critical path: warp 1 (its MMAs wait for the activation
+  // gate anyway) runs the activation one, warp 0 the intermediate one (needed
+  // after the grid barrier; its first weight loads go out a little later).
+  {
+    uint8_t* dq = reinterpret_cast<uint8_t*>(s_dry + kMaxTopK);
+    uint8_t* dsf = reinterpret_cast<uint8_t*>(s_dry + kMaxTopK + 4);
+    if (warp == 1)
+      quantise_share<true>(L.x, L.T, H, k, s_dry, dq, dsf, 1.0f, nullptr, nullptr, true);
+    else if (warp == 0)
+      quantise_share<false>(a1.out, S, I, k, s_dry, dq, dsf, 1.0f, nullptr, nullptr, true);
+  }
   if (warp == 0) {
     if (lane == 0) {
       const int G = static_cast<int>(gridDim.x);
