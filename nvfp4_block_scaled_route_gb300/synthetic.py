@@ -54,8 +54,8 @@ class MoEConfig:
         return self.T * self.k
 
 
-# The five workloads of the benchmark description, plus small and medium
-# parity cases that still span several 128-row tiles with a ragged tail.
+# The five workloads of the benchmark description, plus parity cases that
+# still span several 128-row tiles with a ragged tail.
 CONFIGS = {
     "tiny": MoEConfig("tiny", E=4, H=256, I=128, T=8, k=2,
                       routing="softmax_topk_probs", act_std=1.5,
@@ -72,6 +72,11 @@ CONFIGS = {
     "small": MoEConfig("small", E=6, H=512, I=256, T=97, k=3, routing="zipf"),
     "medium": MoEConfig("medium", E=8, H=1024, I=768, T=600, k=4,
                         routing="zipf"),
+    # ~80 m-tiles x 8 n-tiles in each GEMM: more than four waves of whole
+    # tiles on a 152-SM GPU, the last one partial, still small enough for
+    # the oracle to finish in seconds
+    "waves": MoEConfig("waves", E=8, H=2048, I=1024, T=2464, k=4,
+                       routing="uniform"),
 }
 
 

@@ -167,7 +167,7 @@ def compare(g, ref, cfg, out_dtype=torch.float32, w2=None, topk_w=None):
 
 
 @pytest.mark.parametrize("path", [1, 2], ids=["separate", "fused"])
-@pytest.mark.parametrize("name", ["tiny", "small", "medium"])
+@pytest.mark.parametrize("name", ["tiny", "small", "medium", "waves"])
 def test_forward_matches_oracle(nb, name, path):
     """Both execution paths: three launches (L1, requantise, L2) and the
     single cooperative kernel."""
@@ -187,7 +187,7 @@ def test_forward_matches_oracle(nb, name, path):
     print(f"{name} path {path}: requant flips (scale, nibble) = {flips}")
 
 
-@pytest.mark.parametrize("name", ["small", "medium"])
+@pytest.mark.parametrize("name", ["small", "medium", "waves"])
 def test_paths_agree_bit_for_bit(nb, name):
     """The fused kernel and the three-launch path take the same arithmetic in
     the same order: every intermediate and the output are identical."""
