@@ -1012,48 +1012,63 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
   if (warp == 0) {
     if (lane == 0) {
       const Gate g2{&f.grid_bar[1], 2};
-      if (run_producer(P1, E, tb, bars, smem, pp, abort, nullptr))
-        run_producer(P2, E, tb, bars, smem, pp, abort, &g2);
+      // both phases through one copy of the role's code (the loop is not
+      // unrolled), so that L2 runs instructions L1 has already fetched
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const Phase P = ph ? P2 : P1;
+        if (!run_producer(P, E, tb, bars, smem, pp, abort, ph ? &g2 : nullptr)) break;
+      }
       drain_producer(bars, pp, a1.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      if (run_mma(P1, bars, smem, tmem, pp, abort)) run_mma(P2, bars, smem, tmem, pp, abort);
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const Phase P = ph ? P2 : P1;
+        if (!run_mma(P, bars, smem, tmem, pp, abort)) break;
+      }
       mma_drain(bars, a1.status);
     }
   } else {
     float amax = 0.0f;
-    bool ok = run_epilogue(P1, __ldcg(a1.gs_a), E, tb, bars, tmem, pp, abort, amax, &s_ok,
-                           &s_last);
-    publish_amax(amax, s_amax, a1.amax_partial);
-    if (a1.gs_mid != nullptr) {
-      // static intermediate scale: every tile was requantised by its own CTA;
-      // one barrier (generation 2 opens the producer's L2 activation loads)
-      if (warp == 2 && lane == 0)
-        s_ok = ok && grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
-      epi_bar();
-      ok = s_ok != 0;
-    } else {
-    // barrier 1: every h row and every per-CTA amax is written
-    if (warp == 2 && lane == 0)
-      s_ok = ok && grid_barrier(f.grid_bar, 1, a1.status, abort) ? 1 : 0;
-    epi_bar();
-    ok = s_ok != 0;
-    if (ok) {
-      const float gs = global_scale_from(reduce_partials(a1.amax_partial, gridDim.x));
-      if (blockIdx.x == 0 && warp == 2 && lane == 0) *f.gs_h = gs;
-      requantise(a1, f, tb, E, gs);
-      epi_bar();
-      // barrier 2: hq, its scales and gs_h are written (opens the producer's
-      // activation loads of L2)
-      if (warp == 2 && lane == 0) s_ok = grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
-      epi_bar();
-      ok = s_ok != 0;
+#pragma unroll 1
+    for (int ph = 0; ph < 2; ++ph) {
+      const Phase P = ph ? P2 : P1;
+      // L2: gs_h is final (the requantisation before the second barrier wrote it)
+      bool ok = run_epilogue(P, __ldcg(ph ? a2.gs_a : a1.gs_a), E, tb, bars, tmem, pp, abort,
+                             amax, &s_ok, &s_last);
+      if (ph == 1) break;
+      publish_amax(amax, s_amax, a1.amax_partial);
+      if (a1.gs_mid != nullptr) {
+        // static intermediate scale: every tile was requantised by its own
+        // CTA; one barrier (generation 2 opens the producer's L2 activation
+        // loads)
+        if (warp == 2 && lane == 0)
+          s_ok = ok && grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
+        epi_bar();
+        ok = s_ok != 0;
+      } else {
+        // barrier 1: every h row and every per-CTA amax is written
+        if (warp == 2 && lane == 0)
+          s_ok = ok && grid_barrier(f.grid_bar, 1, a1.status, abort) ? 1 : 0;
+        epi_bar();
+        ok = s_ok != 0;
+        if (ok) {
+          const float gs = global_scale_from(reduce_partials(a1.amax_partial, gridDim.x));
+          if (blockIdx.x == 0 && warp == 2 && lane == 0) *f.gs_h = gs;
+          requantise(a1, f, tb, E, gs);
+          epi_bar();
+          // barrier 2: hq, its scales and gs_h are written (opens the
+          // producer's activation loads of L2)
+          if (warp == 2 && lane == 0)
+            s_ok = grid_barrier(f.grid_bar, 2, a1.status, abort) ? 1 : 0;
+          epi_bar();
+          ok = s_ok != 0;
+        }
+      }
+      if (!ok) break;
     }
-    }
-    // gs_h is final: the requantisation before the second barrier wrote it
-    if (ok)
-      run_epilogue(P2, __ldcg(a2.gs_a), E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
   }
   teardown_cta(bars, tmem);
 }
@@ -1302,13 +1317,23 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
       const int G = static_cast<int>(gridDim.x);
       const Gate g1{&L.grid_bar[3], G};
       const Gate g2{&L.grid_bar[4], G};
-      if (run_producer(P1, E, tb, bars, smem, pp, abort, &g1))
-        run_producer(P2, E, tb, bars, smem, pp, abort, &g2);
+      // both phases through one copy of the role's code (the loop is not
+      // unrolled), so that L2 runs instructions L1 has already fetched
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const Phase P = ph ? P2 : P1;
+        const Gate g = ph ? g2 : g1;
+        if (!run_producer(P, E, tb, bars, smem, pp, abort, &g)) break;
+      }
       drain_producer(bars, pp, a1.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      if (run_mma(P1, bars, smem, tmem, pp, abort)) run_mma(P2, bars, smem, tmem, pp, abort);
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const Phase P = ph ? P2 : P1;
+        if (!run_mma(P, bars, smem, tmem, pp, abort)) break;
+      }
       mma_drain(bars, a1.status);
     }
   } else {
@@ -1386,39 +1411,45 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     float amax = 0.0f;
     // every CTA computed the same gs_x itself (CTA 0's copy in memory is for
     // the caller, with no ordering against this read)
-    bool ok = run_epilogue(P1, s_gs, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
-    publish_amax(amax, s_amax, a1.amax_partial);
-    // the one grid barrier: every h row is written and every CTA's max of |h|
-    // is folded into one word (non-negative floats order like their bits)
-    if (lead) {
-      s_ok = 0;
-      if (ok) {
-        const float cta_max = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
-        atomicMax(&L.grid_bar[5], __float_as_int(cta_max));
-        s_ok = count_barrier(&L.grid_bar[0], a1.status, abort) ? 1 : 0;
+    // L1 and L2 run through one copy of the epilogue code (see the producer)
+    const YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
+                     s_scratch, &s_n};
+    float gs_phase = s_gs;
+#pragma unroll 1
+    for (int ph = 0; ph < 2; ++ph) {
+      const Phase P = ph ? P2 : P1;
+      bool ok = run_epilogue(P, gs_phase, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last,
+                             ph ? &yr : nullptr);
+      if (ph == 1) break;
+      publish_amax(amax, s_amax, a1.amax_partial);
+      // the one grid barrier: every h row is written and every CTA's max of
+      // |h| is folded into one word (non-negative floats order like their bits)
+      if (lead) {
+        s_ok = 0;
+        if (ok) {
+          const float cta_max = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
+          atomicMax(&L.grid_bar[5], __float_as_int(cta_max));
+          s_ok = count_barrier(&L.grid_bar[0], a1.status, abort) ? 1 : 0;
+        }
       }
-    }
-    epi_bar();
-    ok = s_ok != 0;
-    if (ok && a1.gs_mid != nullptr) {
-      // static intermediate scale: no global max; the share of h is
-      // requantised with the scale of each slot's expert
-      quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, 0.0f, a1.gs_mid, L.topk_ids);
+      epi_bar();
+      if (s_ok == 0) {
+        // the producer's wait for the h shares ends at once
+        if (lead) *abort = 1;
+        break;
+      }
+      if (a1.gs_mid != nullptr) {
+        // static intermediate scale: no global max; the share of h is
+        // requantised with the scale of each slot's expert
+        quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, 0.0f, a1.gs_mid, L.topk_ids);
+        gs_phase = 0.0f;
+      } else {
+        const float gs = global_scale_from(__int_as_float(ld_acquire(&L.grid_bar[5])));
+        if (blockIdx.x == 0 && lead) *L.gs_h = gs;
+        quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, gs);
+        gs_phase = gs;
+      }
       share_done(&L.grid_bar[4]);
-      YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
-                 s_scratch, &s_n};
-      run_epilogue(P2, 0.0f, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
-    } else if (ok) {
-      const float gs = global_scale_from(__int_as_float(ld_acquire(&L.grid_bar[5])));
-      if (blockIdx.x == 0 && lead) *L.gs_h = gs;
-      quantise_share<false>(a1.out, S, I, k, s_row, L.hq, L.hsf, gs);
-      share_done(&L.grid_bar[4]);
-      YReduce yr{L.ycnt, L.topk_w, s_row, s_tok, L.y, L.y_dtype, k, a2.n_tiles,
-                 s_scratch, &s_n};
-      run_epilogue(P2, gs, E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last, &yr);
-    } else if (lead) {
-      // the producer's wait for the h shares ends at once
-      *abort = 1;
     }
   }
   teardown_cta(bars, tmem);
