@@ -89,3 +89,44 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     # reduce: bad dtype, bad H
     assert lib.moe_unpermute_reduce(fake, fake, fake, 2, 2, 64, fake, 5, None) == 1
     assert lib.moe_unpermute_reduce(fake, fake, fake, 2, 2, 60, fake, 0, None) == 2
+
+
+def test_router_and_layer_arguments_are_rejected_on_the_host(lib):
+    """The router and the one-call layer entry point fail their argument
+    checks before anything is enqueued (no GPU needed)."""
+    from nvfp4_block_scaled_route_gb300 import binding
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced
+    big = 1 << 30
+    sel = binding.ROUTER_SELECTED
+    # router: k > E, k > 32, E > 256, bad softmax mode
+    assert lib.moe_router_topk(fake, fake, 4, 256, 6, 7, sel, fake, fake, fake, big, None) == 1
+    assert lib.moe_router_topk(fake, fake, 4, 256, 64, 33, sel, fake, fake, fake, big, None) == 1
+    assert lib.moe_router_topk(fake, fake, 4, 256, 257, 8, sel, fake, fake, fake, big, None) == 1
+    assert lib.moe_router_topk(fake, fake, 4, 256, 48, 8, 9, fake, fake, fake, big, None) == 1
+    # router: H not a multiple of 128; T = 0 is a no-op
+    assert lib.moe_router_topk(fake, fake, 4, 192, 48, 8, sel, fake, fake, fake, big, None) == 2
+    assert lib.moe_router_topk(None, None, 0, 256, 48, 8, sel, None, None, None, 0, None) == 0
+    # router: misaligned x, workspace too small
+    assert lib.moe_router_topk(P((1 << 20) + 2), fake, 4, 256, 48, 8, sel, fake, fake, fake, big,
+                               None) == 3
+    assert lib.moe_router_topk(fake, fake, 4096, 7168, 48, 8, sel, fake, fake, fake, 16,
+                               None) == 4
+    assert lib.moe_router_workspace_size(4096, 7168, 48) > 16
+    # layer: bad x / y dtype, unsupported H, null workspace, misaligned y,
+    # workspace too small; T = 0 is a no-op
+    w = binding.Weights(48, 7168, 3072, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)
+    wh = binding.Weights(48, 7000, 3072, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)
+    need = lib.moe_nvfp4_layer_workspace_size(1, 8, 48, 7168, 3072)
+    assert need > lib.moe_nvfp4_workspace_size(1, 8, 48, 7168, 3072)
+    args = lambda wt, xd, y, yd, ws, n: (ctypes.byref(wt), fake, xd, fake, fake, 1, 8, y, yd,
+                                         None, ws, n, None)
+    assert lib.moe_nvfp4_layer_forward(*args(w, 5, fake, 0, fake, need)) == 1
+    assert lib.moe_nvfp4_layer_forward(*args(w, 0, fake, 9, fake, need)) == 1
+    assert lib.moe_nvfp4_layer_forward(*args(wh, 0, fake, 0, fake, need)) == 2
+    assert lib.moe_nvfp4_layer_forward(*args(w, 0, fake, 0, None, need)) == 1
+    assert lib.moe_nvfp4_layer_forward(*args(w, 0, P((1 << 20) + 8), 0, fake, need)) == 3
+    assert lib.moe_nvfp4_layer_forward(*args(w, 0, fake, 0, fake, need - 16)) == 4
+    assert lib.moe_nvfp4_layer_forward(ctypes.byref(w), None, 0, None, None, 0, 8, None, 0, None,
+                                       fake, lib.moe_nvfp4_layer_workspace_size(0, 8, 48, 7168,
+                                                                                3072), None) == 0
