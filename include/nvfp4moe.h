@@ -19,7 +19,10 @@
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
  *    stated otherwise.  The library never allocates or frees device memory,
  *    never synchronises the host and keeps no state between calls except a
- *    per-device cache of kernel attributes.
+ *    cache of kernel attributes (the GEMM kernels' shared-memory size, set
+ *    on the first launch; this cache is process-wide, so a process that
+ *    uses these entry points should drive one GPU) and the per-device
+ *    address of the allocation-free routing array.
  *  - Work is enqueued on `stream`; a call returns once its kernels are
  *    enqueued.  Calls are stream-ordered and may be captured in a CUDA graph.
  *  - The return value is an nvmoe_status.  Host-side argument checks run
