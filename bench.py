@@ -10,16 +10,23 @@ launches above that (the library counts its own launches).  The step is
 replayed as one CUDA graph.  --api calls times the four-call composition
 (route, quantise, forward, reduce) instead.
 
-Default workload: the one-token decode case (E=48 experts, H=7168, I=3072,
-top-8), whose roofline is HBM bandwidth on the weight + scale bytes of the
-experts that receive a token.  The L2 cache is flushed (256 MiB write)
-before every timed step; inputs are resident in HBM before the timed region.
+Default workload: the large prefill case (E=48 experts, H=7168, I=3072,
+T=16384 tokens, top-8 with one expert in every token's list and six experts
+idle, Student-t activations), the largest of the workloads, whose roofline is
+the dense FP4 tensor peak.  --config decode1 (one token) and the others
+select the smaller workloads; decode workloads are bound by HBM bandwidth on
+the weight + scale bytes of the experts that receive a token.  The L2 cache
+is flushed (256 MiB write) before every timed step; inputs are resident in
+HBM before the timed region.
 
 Also reported:
   roofline      the dominant kernel (the single layer kernel for small batches,
                 else the L1 GEMM) timed alone with CUDA events recorded by
-                the library on the launching stream, against the
-                measured HBM copy bandwidth (MEASURED_PEAKS.json)
+                the library on the launching stream, against the measured
+                HBM copy bandwidth (MEASURED_PEAKS.json) for decode, and for
+                prefill against the dense FP4 tensor peak that the library's
+                own probe (nvmoe_fp4_mma_probe) measures on this GPU, with the
+                datasheet figure beside it
   e2e           the same metric through the public API from pinned host
                 buffers: H2D of x / topk ids / topk weights, forward, D2H of y
   cpu_baseline  the CPU oracle (numpy, fp64) timed on a bounded sample of the
@@ -49,16 +56,17 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/sec on 1 GB300; % HBM roofline (decode), % FP4 TC peak (prefill)"
 UNIT = "tokens/s"
 FLUSH_BYTES = 256 << 20            # > 129 MB L2
-FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / BF16 tensor ratio on GB300
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: 2000 for decode workloads, 200 for prefill)")
+    p.add_argument("--warmup", type=int, default=None,
+                   help="untimed warm-up steps (default: 50 decode, 10 prefill)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="decode1")
+    p.add_argument("--config", default="prefill16k")
     p.add_argument("--api", choices=["layer", "calls"], default="layer",
                    help="one-call layer entry point, or route/quantise/forward/reduce")
     p.add_argument("--gate-up-scales", choices=["joint", "split"], default="joint",
@@ -66,13 +74,20 @@ def parse():
     p.add_argument("--mid-scale", choices=["dynamic", "static"], default="dynamic",
                    help="the pages' dynamic intermediate scale, or a static per-expert one "
                         "(calibrated as one dynamic forward's scale)")
-    p.add_argument("--part", choices=["layer", "router"], default="layer",
-                   help="the MoE layer (steps 1-7), or the router front-end alone")
+    p.add_argument("--part", choices=["layer", "router", "peak"], default="layer",
+                   help="the MoE layer (steps 1-7), the router front-end alone, or the "
+                        "dense FP4 tensor-core probe alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
                    help="run this many eager steps and exit (for ncu launch lists)")
-    return p.parse_args()
+    a = p.parse_args()
+    big = a.config.startswith("prefill")
+    if a.steps is None:
+        a.steps = 200 if big else 2000
+    if a.warmup is None:
+        a.warmup = 10 if big else 50
+    return a
 
 
 def peaks():
@@ -143,87 +158,56 @@ class ClockSampler:
 
 
 # ------------------------------------------------------- oracle sample ----
-_SAMPLE_CACHE = {}
+def oracle_sample(cfg, n_tok, x_h=None, ids_h=None, w_h=None, weight_device=None):
+    """Inputs of a CPU-oracle sample and a function that times one pass.
 
-
-def _oracle_sample_worker(args):
-    """Time the oracle on `n_slots` slots of one token, each restricted to `c`
-    of the I intermediate columns (L1: c gate + c up columns; L2: c of the I
-    reduction rows), so the work is the fraction n_slots*c/(I*k) of one
-    token.  Runs in a spawned process with one BLAS thread."""
-    cfgname, c, n_slots, seed = args
+    The sample is the first n_tok tokens of the workload (activations and
+    routing as drawn for the whole batch) with the workload's weights of the
+    experts those tokens use: drawn by the seeded generator on
+    `weight_device` (the GPU, i.e. the values the GPU arm quantises; the
+    host when there is none) and quantised by the oracle (set-up, untimed).
+    One pass is the C++ oracle's whole forward (route, quantise, L1 with
+    alpha, SiLU*up, requantise, L2 with alpha, weighted reduce) on all host
+    cores; it returns the seconds of that pass."""
     import numpy as np
     import torch
-    from oracle import moe as omoe
-    from oracle import nvfp4 as onv
+    from oracle import cpp as ocpp
     from nvfp4_block_scaled_route_gb300 import synthetic as syn
-    cfg = syn.CONFIGS[cfgname]
-    H, I = cfg.H, cfg.I
-    # the sample's weights are drawn and quantised once per (workload, slice)
-    # and kept by the worker: that set-up is not the oracle's forward work
-    key = (cfgname, c, n_slots)
-    if key not in _SAMPLE_CACHE:
-        g = torch.Generator().manual_seed(seed)
-        x = syn.draw_activations(cfg, T=1).float().numpy()
-        slots = []
-        for s in range(n_slots):
-            std = cfg.w_std * (0.5 + 1.5 * float(torch.rand(1, generator=g)))
-            w1 = (torch.randn((H, 2 * c), generator=g) * std).numpy()
-            w2 = (torch.randn((c, H), generator=g) * std).numpy()
-            slots.append((onv.quantize_weight(w1), onv.quantize_weight(w2)))
-        _SAMPLE_CACHE.clear()
-        _SAMPLE_CACHE[key] = (x, slots)
-    x, slots = _SAMPLE_CACHE[key]
-    t0 = time.perf_counter()
-    xq, xsf, gsx = onv.quantize_rows(x)
-    y = np.zeros((1, H))
-    for (q1, s1, g1), (q2, s2, g2) in slots:
-        l1 = omoe.expert_l1(xq, xsf, gsx, q1, s1, g1)
-        h = omoe.swiglu(l1)
-        hq, hsf, gsh = onv.quantize_rows(h)
-        y += 0.125 * omoe.expert_l2(hq, hsf, gsh, q2, s2, g2)
-    t1 = time.perf_counter()
-    return t1 - t0, n_slots * c / (I * cfg.k)
+    if x_h is None:
+        x_h = syn.draw_activations(cfg)
+        ids_h, w_h = syn.draw_routing(cfg)
+    x = x_h[:n_tok].float().numpy()
+    ids = ids_h[:n_tok].numpy()
+    w = w_h[:n_tok].numpy()
+    used = sorted(set(ids.reshape(-1).tolist()))
+    E, H, I = cfg.E, cfg.H, cfg.I
+    W1q = np.zeros((E, H // 2, 2 * I), np.uint8)
+    W1s = np.zeros((E, H // 16, 2 * I), np.uint8)
+    W2q = np.zeros((E, I // 2, H), np.uint8)
+    W2s = np.zeros((E, I // 16, H), np.uint8)
+    g1 = np.ones(E, np.float32)
+    g2 = np.ones(E, np.float32)
+    dev = weight_device if weight_device is not None else "cpu"
+    for e in used:
+        W1q[e], W1s[e], g1[e] = ocpp.nvfp4.quantize_weight(
+            syn.draw_weight(cfg, 1, e, device=dev).cpu().numpy())
+        W2q[e], W2s[e], g2[e] = ocpp.nvfp4.quantize_weight(
+            syn.draw_weight(cfg, 2, e, device=dev).cpu().numpy())
+    if dev != "cpu":
+        torch.cuda.empty_cache()
+
+    def one_pass():
+        return ocpp.moe.forward(x, ids, w, W1q, W1s, g1, W2q, W2s, g2)["seconds"]
+
+    desc = (f"the first {n_tok} token(s) of the workload ({len(used)} experts) through the "
+            f"C++ oracle's whole forward (fp64 GEMMs), the workload's own weights "
+            f"(drawn on {'the GPU' if dev != 'cpu' else 'the host'}), "
+            f"{ocpp.threads()} OpenMP threads")
+    return one_pass, ocpp.threads(), desc
 
 
-class OracleRunner:
-    """One spawned worker process (one BLAS thread) that runs oracle samples."""
-
-    ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
-
-    def __enter__(self):
-        old = {k: os.environ.get(k) for k in self.ENV}
-        os.environ.update(self.ENV)
-        try:
-            self.pool = mp.get_context("spawn").Pool(1)
-        finally:
-            for k, v in old.items():
-                if v is None:
-                    os.environ.pop(k, None)
-                else:
-                    os.environ[k] = v
-        return self
-
-    def __exit__(self, *exc):
-        self.pool.close()
-        self.pool.join()
-
-    def sample(self, cfgname: str, c: int, n_slots: int, seed: int = 0):
-        return self.pool.apply(_oracle_sample_worker, ((cfgname, c, n_slots, seed),))
-
-    def sized(self, cfgname: str, budget_s: float, seed: int = 0):
-        """Slice width and slot count so that one sample takes about budget_s."""
-        from nvfp4_block_scaled_route_gb300 import synthetic as syn
-        cfg = syn.CONFIGS[cfgname]
-        c0 = 64
-        t, _ = self.sample(cfgname, c0, 1, seed)
-        per_col = max(t / c0, 1e-6)
-        c = int(budget_s / per_col) // 64 * 64
-        n_slots = 1
-        if c > cfg.I:
-            n_slots = min(cfg.k, max(1, int(c // cfg.I)))
-            c = cfg.I
-        return max(64, c), n_slots
+def oracle_tokens(cfg, budget_tokens: int) -> int:
+    return max(1, min(cfg.T, budget_tokens))
 
 
 # ---------------------------------------------------------------- main ----
@@ -233,33 +217,31 @@ def workload_desc(cfg):
 
 
 def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores: each step one pass of
+    the C++ oracle over a one-token sample of the workload (its token, its
+    routing, the workload's weights of its experts)."""
     from nvfp4_block_scaled_route_gb300 import synthetic as syn
+    import torch
     cfg = syn.CONFIGS[args.config]
     if rank != 0:
         return
-    total_steps = args.steps + args.warmup
-    budget = max(0.05, min(20.0, 120.0 / max(total_steps, 1)))
-    times, units = [], []
-    with OracleRunner() as runner:
-        c, n_slots = runner.sized(args.config, budget)
-        for i in range(total_steps):
-            t, u = runner.sample(args.config, c, n_slots, seed=i)
-            if i >= args.warmup:
-                times.append(t)
-                units.append(u)
-    tok = sum(units)
+    n_tok = oracle_tokens(cfg, 1)
+    dev = "cuda" if torch.cuda.is_available() else None
+    one_pass, cores, desc = oracle_sample(cfg, n_tok, weight_device=dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = one_pass()
+        if i >= args.warmup:
+            times.append(t)
     sec = sum(times)
-    value = tok / sec
+    value = n_tok * len(times) / sec
     ms = 1000.0 * sec / max(len(times), 1)
-    sample = (f"per step: {n_slots} slot(s) of one token, {c} of I={cfg.I} intermediate "
-              f"columns (fraction {units[0]:.5f} of a token); value = tokens-equivalent / "
-              f"oracle seconds")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": workload_desc(cfg)},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -310,6 +292,70 @@ def run_router(args, nb, syn, cfg, dev, world, torch):
                          "frac": achieved / hbm_gbs, "peak_source": peak_src,
                          "algorithmic_bytes_per_step": nbytes}}
     print(json.dumps(line), flush=True)
+
+
+FP4_DATASHEET_TFLOPS = 13500.0       # GB300 dense NVFP4, nominal (no sparsity)
+
+
+def measure_fp4_peak(nb, torch, dev, sustain_s: float = 2.0):
+    """Dense NVFP4 tensor-core peak of this GPU from the library's own probe
+    (tcgen05.mma kind::mxf4nvf4 back to back on every SM, operands resident
+    in shared memory).  Burst: the best single launch of the faster of the
+    one-CTA and CTA-pair forms; sustained: that form launched back to back
+    for `sustain_s` seconds (under the power cap)."""
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    grid = n_sm - (n_sm & 1)
+    iters = 16384
+    forms = {}
+    for variant, name in ((0, "one CTA, M=128 N=256"), (1, "CTA pair, M=256 N=256")):
+        r = nb.fp4_mma_probe(variant, iters=iters, grid=grid, repeats=5, device=dev)
+        if r["status"] != 0:
+            raise RuntimeError(f"FP4 probe variant {variant} status {r['status']}")
+        forms[name] = r
+    best_name = max(forms, key=lambda n: forms[n]["tflops"])
+    best = forms[best_name]
+    # sustained: back-to-back launches of the best form
+    per_launch_s = min(best["ms"]) / 1e3
+    n = max(10, int(sustain_s / per_launch_s))
+    cycles = torch.zeros(grid, dtype=torch.int64, device=dev)
+    ws = nb._workspace(256, dev)
+    s = torch.cuda.Stream(device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record(s)
+        for _ in range(n):
+            nb._check("nvmoe_fp4_mma_probe", nb.lib().nvmoe_fp4_mma_probe(
+                best["variant"], iters, grid, nb._ptr(cycles), nb._ptr(ws), ws.numel(),
+                s.cuda_stream))
+        b.record(s)
+    s.synchronize()
+    sustained = n * grid * iters * 2.0 * 128 * 256 * 64 / (a.elapsed_time(b) / 1e3) / 1e12
+    return {"burst_tflops": best["tflops"], "sustained_tflops": sustained, "form": best_name,
+            "cycles_per_mma": best["cycles_per_mma"],
+            "forms": {k: {"tflops": v["tflops"], "cycles_per_mma": v["cycles_per_mma"]}
+                      for k, v in forms.items()},
+            "datasheet_tflops": FP4_DATASHEET_TFLOPS}
+
+
+def run_peak(args, nb, dev, torch):
+    """The probe alone: every variant, one JSON line."""
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    grid = n_sm - (n_sm & 1)
+    names = {0: "1cta_n256", 1: "pair_n256", 2: "1cta_n128", 3: "pair_n128",
+             4: "1cta_n256_cp32", 5: "pair_n256_cp32", 6: "1cta_n128_cp32",
+             7: "pair_n128_cp32", 8: "1cta_n256_cp256", 9: "pair_n256_cp256",
+             10: "1cta_n128_cp256", 11: "pair_n128_cp256"}
+    out = {}
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for v, name in names.items():
+        r = nb.fp4_mma_probe(v, iters=16384, grid=grid, repeats=5, device=dev)
+        out[name] = {"tflops": round(r["tflops"], 1), "cycles_per_mma": r["cycles_per_mma"],
+                     "status": r["status"]}
+    pk = measure_fp4_peak(nb, torch, dev)
+    clocks = sampler.stop()
+    print(json.dumps({"metric": "dense NVFP4 tensor-core throughput (probe)", "unit": "TFLOP/s",
+                      "variants": out, "peak": pk, "clocks": clocks, "grid": grid}), flush=True)
 
 
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "quant.cuh", "internal.h")
@@ -377,6 +423,12 @@ def main():
     cfg = syn.CONFIGS[args.config]
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.part == "peak":
+        if rank == 0:
+            run_peak(args, nb, dev, torch)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.part == "router":
         run_router(args, nb, syn, cfg, dev, world, torch)
         if world > 1:
@@ -439,7 +491,7 @@ def main():
     l2_bytes = E_act * (H * I // 2 + H * I // 16)
     S = cfg.T * cfg.k
     flops = 2.0 * S * H * 2 * I + 2.0 * S * I * H
-    hbm_gbs, bf16_tf, peak_src = peaks()
+    hbm_gbs, _, peak_src = peaks()
 
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -538,11 +590,19 @@ def main():
     else:
         l1_flops = 2.0 * S * H * 2 * I
         achieved = l1_flops / (l1_ms / 1000.0) / 1e12
-        peak = bf16_tf * FP4_OVER_BF16
+        fp4 = measure_fp4_peak(nb, torch, dev)
+        peak = fp4["burst_tflops"]
+        step_tflops = flops / (ms_per_step / 1000.0) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} bf16 x {FP4_OVER_BF16} nominal fp4/bf16",
+                "frac": achieved / peak,
+                "peak_source": "measured: nvmoe_fp4_mma_probe burst (" + fp4["form"] + ")",
+                "peak_sustained": fp4["sustained_tflops"],
+                "peak_datasheet": fp4["datasheet_tflops"],
+                "frac_of_datasheet": achieved / fp4["datasheet_tflops"],
+                "probe": fp4,
                 "kernel": "grouped_gemm_kernel (L1, mode 1)",
-                "algorithmic_flops_per_launch": l1_flops, "launch_ms": l1_ms}
+                "algorithmic_flops_per_launch": l1_flops, "launch_ms": l1_ms,
+                "step_tflops": step_tflops, "step_frac": step_tflops / peak}
     roof["traffic"] = profiled_traffic(roof["kernel"].split()[0], args.config)
     step_bytes = l1_bytes + l2_bytes
 
@@ -581,12 +641,13 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        with OracleRunner() as runner:
-            c, n_slots = runner.sized(args.config, 15.0)
-            t, u = runner.sample(args.config, c, n_slots, seed=1)
-        cpu = {"value": u / t, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n_slots} slot(s) of one token, {c} of I={I} intermediate columns "
-                         f"= {u:.5f} token-equivalents in {t:.2f} s (numpy, 1 thread)"}
+        del layer, pw
+        torch.cuda.empty_cache()
+        n_tok = oracle_tokens(cfg, 4)
+        one_pass, cores, desc = oracle_sample(cfg, n_tok, x_h, ids_h, w_h, weight_device=dev)
+        t = one_pass()
+        cpu = {"value": n_tok / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{desc}: {t:.2f} s"}
 
     if rank == 0:
         line = {

@@ -19,10 +19,10 @@
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
  *    stated otherwise.  The library never allocates or frees device memory,
  *    never synchronises the host and keeps no state between calls except a
- *    cache of kernel attributes (the GEMM kernels' shared-memory size, set
- *    on the first launch; this cache is process-wide, so a process that
- *    uses these entry points should drive one GPU) and the per-device
- *    address of the allocation-free routing array.
+ *    per-device cache of kernel attributes (each kernel's shared-memory size,
+ *    set on its first launch on a device) and the per-device address of the
+ *    allocation-free routing array.  One process may drive several GPUs:
+ *    every call works on the current device.
  *  - Work is enqueued on `stream`; a call returns once its kernels are
  *    enqueued.  Calls are stream-ordered and may be captured in a CUDA graph.
  *  - The return value is an nvmoe_status.  Host-side argument checks run
@@ -79,7 +79,8 @@ typedef enum { NVMOE_BF16 = 0, NVMOE_F32 = 1 } nvmoe_dtype;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvmoe_status_str(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 200 (nvmoe_taps gained the
+ * ready-flag members). */
 int nvmoe_version(void);
 
 /* Number of kernels this library has enqueued in this process so far (all
@@ -97,6 +98,37 @@ int nvmoe_clear_status(void* workspace, cudaStream_t stream);
 /* Size in bytes of a staged (MMA layout) block-scale buffer for `rows` rows
  * of `cols` elements. */
 size_t nvfp4_sf_mma_bytes(int64_t rows, int64_t cols);
+
+/* ------------------------------------------------------- measurement --
+ * nvmoe_fp4_mma_probe — dense NVFP4 tensor-core throughput probe.  No
+ * counterpart in the source pages: the workloads' prefill figure is a
+ * fraction of the dense FP4 tensor peak, and this measures that peak on the
+ * GPU at hand instead of taking a datasheet number.  Each CTA issues `iters`
+ * back-to-back tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X (K = 64
+ * each, operands resident in shared memory, fp32 accumulator in TMEM) and
+ * records the SM clock cycles from its first issue to the completion of the
+ * last MMA.  FLOPs per CTA = iters * 2 * 128 * N * 64 (N = 256, or 128 with
+ * bit 2); the caller times the launch with CUDA events.
+ *   variant  bit 1: CTA pairs (cta_group::2, M = 256 over two SMs); bit 2:
+ *            N = 128; bit 4: per MMA the 32x128b.warpx4 scale copies of a
+ *            one-atom-per-k-block staging (1 for A, N/128 for B); bit 8: per
+ *            four MMAs 128x256b scale copies (1 for A, N/64 for B).  Bits 4
+ *            and 8 are exclusive.  Bit 16: the MMAs alternate between two
+ *            accumulators; bit 32 (N = 128 only): between four; bit 64: no
+ *            MMA adds to the previous one's result; bit 128: the scale
+ *            copies alone (with bit 4 or 8), no MMA; with bit 8, bit 256:
+ *            only the A copy, bit 512: the next four MMAs' copies issued
+ *            after the second MMA of the current four.  Bit 1024 (with at
+ *            most bit 2; iters a multiple of 4): one CTA whose scales reach
+ *            TMEM by tcgen05.st from four warps, a stage of four MMAs at a
+ *            time, while a fifth warp issues the MMAs.
+ *   iters    1 .. 2^20;  grid  CTAs (even with bit 1), one per SM at most
+ *   cycles   int64 [grid] out (device): cycles of each issuing CTA (-1 for
+ *            the odd CTA of a pair)
+ *   workspace  >= 256 bytes, zeroed; its first word is the status word
+ * Operand values are fixed (E2M1 1.0, scales 1.0); nothing else is read. */
+int nvmoe_fp4_mma_probe(int variant, int iters, int grid, long long* cycles,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- step 1 --
  * moe_route_permute — per-expert histogram, prefix sum and stable slot
@@ -283,6 +315,18 @@ typedef struct {
   cudaEvent_t stage_events[4];
   int path;
   int32_t* slot_of;       /* moe_nvfp4_layer_forward: int32 [T*k] row of each slot */
+  /* moe_nvfp4_forward only (moe_nvfp4_layer_forward rejects it with
+   * NVMOE_ERR_INVALID_ARG): the activation rows xq / xsf_mma are produced by
+   * another stream or device and are ready once *ready_flag >= ready_value
+   * (an int32 device word; gs_x and the routing tables must be ready at
+   * launch).  The L1 kernel waits for the flag before its first load, at
+   * most ready_wait_us microseconds (<= 0: 2 s); a wait that runs out
+   * records NVMOE_ERR_TIMEOUT in the workspace status word and the call's
+   * kernels return without producing results.  The workspace is left ready
+   * for the next call.  NULL = ready at launch. */
+  const int32_t* ready_flag;
+  int ready_value;
+  int ready_wait_us;
 } nvmoe_taps;
 
 /* moe_nvfp4_forward — the expert FFN on grouped slots ("NVFP4 MegaMoE Debug

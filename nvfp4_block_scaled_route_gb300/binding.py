@@ -41,7 +41,8 @@ class Taps(ctypes.Structure):
     _fields_ = [("l1_out", ctypes.c_void_p), ("h", ctypes.c_void_p), ("hq", ctypes.c_void_p),
                 ("hsf_mma", ctypes.c_void_p), ("gs_h", ctypes.c_void_p),
                 ("stage_events", ctypes.c_void_p * 4), ("path", ctypes.c_int),
-                ("slot_of", ctypes.c_void_p)]
+                ("slot_of", ctypes.c_void_p), ("ready_flag", ctypes.c_void_p),
+                ("ready_value", ctypes.c_int), ("ready_wait_us", ctypes.c_int)]
 
 
 PATH_AUTO, PATH_SEPARATE, PATH_FUSED, PATH_LAYER = 0, 1, 2, 3
@@ -56,6 +57,7 @@ SIGNATURES = {
     "nvmoe_read_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "nvmoe_clear_status": (_I, [_P, _P]),
     "nvfp4_sf_mma_bytes": (_SZ, [_I64, _I64]),
+    "nvmoe_fp4_mma_probe": (_I, [_I, _I, _I, _P, _P, _SZ, _P]),
     "moe_route_rows_bound": (_I64, [_I64, _I, _I]),
     "moe_route_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_route_permute": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -99,10 +101,16 @@ def _check(fn: str, status: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    """Device address of a tensor's data.  The library reads and writes
+    every buffer as dense row-major memory, so a tensor with other strides
+    (a transposed or sliced view) is refused rather than passed as if it
+    were dense."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor (the library reads dense row-major memory)")
     return t.data_ptr()
 
 
@@ -128,6 +136,42 @@ def read_status(ws: torch.Tensor, stream=None) -> int:
     out = ctypes.c_int(0)
     _check("nvmoe_read_status", lib().nvmoe_read_status(_ptr(ws), _stream(stream), ctypes.byref(out)))
     return out.value
+
+
+# ------------------------------------------------------------ measurement --
+PROBE_PAIR, PROBE_N128, PROBE_CP32, PROBE_CP256 = 1, 2, 4, 8
+
+
+def fp4_mma_probe(variant: int, iters: int, grid: int, repeats: int = 3, device=None,
+                  stream=None):
+    """Dense NVFP4 tensor-core throughput (nvmoe_fp4_mma_probe).
+
+    Runs the probe `repeats` times on `stream`, each launch timed with CUDA
+    events on that stream.  Returns a dict: best-launch TFLOP/s, the median
+    cycles per MMA of the issuing CTAs, the launch times (ms) and the status."""
+    dev = torch.device(device if device is not None else "cuda")
+    cycles = torch.zeros(grid, dtype=torch.int64, device=dev)
+    ws = _workspace(256, dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    N = 128 if variant & PROBE_N128 else 256
+    flops = float(grid) * iters * 2.0 * 128 * N * 64
+    ms = []
+    with torch.cuda.stream(s):
+        for _ in range(repeats):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            _check("nvmoe_fp4_mma_probe", lib().nvmoe_fp4_mma_probe(
+                variant, iters, grid, _ptr(cycles), _ptr(ws), ws.numel(), s.cuda_stream))
+            b.record(s)
+            s.synchronize()
+            ms.append(a.elapsed_time(b))
+    c = cycles.cpu()
+    c = c[c > 0].double()
+    return {"variant": variant, "iters": iters, "grid": grid, "N": N,
+            "tflops": flops / (min(ms) / 1e3) / 1e12, "ms": ms,
+            "cycles_per_mma": float(c.median() / iters) if c.numel() else None,
+            "status": read_status(ws)}
 
 
 # ------------------------------------------------------------------ step 1 --
@@ -297,6 +341,9 @@ def _taps(taps: Optional[dict]):
             t.stage_events[i] = ev.cuda_event
     t.path = int(taps.get("path", PATH_AUTO))
     t.slot_of = _ptr(taps.get("slot_of"))
+    t.ready_flag = _ptr(taps.get("ready_flag"))
+    t.ready_value = int(taps.get("ready_value", 0))
+    t.ready_wait_us = int(taps.get("ready_wait_us", 0))
     return t
 
 

@@ -87,6 +87,12 @@ cudaError_t counted(cudaError_t e, int kernels) {
   return e;
 }
 
+}  // namespace
+
+void nvmoe::note_launches(int kernels) { g_launches += kernels; }
+
+namespace {
+
 // Workspace carving helper.
 struct Carve {
   uint8_t* base;
@@ -98,6 +104,15 @@ struct Carve {
     return p;
   }
 };
+
+// T*k < 2^31 (slot indices are int32), checked without forming the product,
+// which could overflow int64 for a huge T.
+bool slots_fit(int64_t T, int k) { return k >= 1 && T <= int64_t{INT32_MAX} / k; }
+
+// rows * cols elements below 2^40, checked without forming the product.
+bool elems_fit(int64_t rows, int64_t cols) {
+  return cols <= 0 || rows <= (int64_t{1} << 40) / cols;
+}
 
 int64_t rows_bound(int64_t T, int k, int E) {
   const int64_t S = T * k;
@@ -123,7 +138,7 @@ const char* nvmoe_status_str(int s) {
   }
 }
 
-int nvmoe_version(void) { return 100; }
+int nvmoe_version(void) { return 200; }
 
 uint64_t nvmoe_kernel_launch_count(void) { return g_launches.load(); }
 
@@ -147,14 +162,38 @@ size_t nvfp4_sf_mma_bytes(int64_t rows, int64_t cols) {
   return sf_mma_bytes(rows, cols);
 }
 
+// ------------------------------------------------------- FP4 probe ----
+int nvmoe_fp4_mma_probe(int variant, int iters, int grid, long long* cycles, void* ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+  if (variant < 0 || variant > 2047 || ((variant & kProbeCp32) && (variant & kProbeCp256)))
+    return NVMOE_ERR_INVALID_ARG;
+  // four accumulators of 128 columns fill the 512 TMEM columns: N = 128 only
+  if ((variant & kProbeAcc4) && (!(variant & kProbeN128) || (variant & kProbeAcc2)))
+    return NVMOE_ERR_INVALID_ARG;
+  if ((variant & kProbeNoMma) && !(variant & (kProbeCp32 | kProbeCp256)))
+    return NVMOE_ERR_INVALID_ARG;
+  if ((variant & (kProbeCpAOnly | kProbeCpEarly)) && !(variant & kProbeCp256))
+    return NVMOE_ERR_INVALID_ARG;
+  // the tcgen05.st form: one CTA, whole stages of four MMAs, no other flags
+  if ((variant & kProbeSt) && ((variant & ~(kProbeSt | kProbeN128)) || (iters % 4) != 0))
+    return NVMOE_ERR_INVALID_ARG;
+  if (iters < 1 || iters > (1 << 20) || grid < 1 || grid > 65535 || cycles == nullptr ||
+      ws == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if ((variant & kProbePair) && (grid & 1)) return NVMOE_ERR_INVALID_ARG;
+  if (ws_bytes < kStatusBytes) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  return status_of(counted(launch_mma_probe(variant, iters, grid, cycles, static_cast<int*>(ws),
+                                            stream), 1));
+}
+
 // ------------------------------------------------------------- route ----
 int64_t moe_route_rows_bound(int64_t T, int k, int E) {
-  if (T < 0 || k < 1 || E < 1) return 0;
+  if (T < 0 || k < 1 || E < 1 || !slots_fit(T, k)) return 0;
   return rows_bound(T, k, E);
 }
 
 size_t moe_route_workspace_size(int64_t T, int k, int E) {
-  if (T < 0 || k < 1 || E < 1) return 0;
+  if (T < 0 || k < 1 || E < 1 || !slots_fit(T, k)) return 0;
   const int64_t S = T * k;
   const int64_t chunks = S > 0 ? ceil_div(S, route_chunk_elems()) : 1;
   return kStatusBytes + align_up(static_cast<size_t>(chunks) * E * sizeof(int32_t));
@@ -164,7 +203,7 @@ int moe_route_permute(const int32_t* topk_ids, int64_t T, int k, int E, int32_t*
                       int32_t* expert_counts, int32_t* row_token, int32_t* slot_of, void* ws,
                       size_t ws_bytes, cudaStream_t stream) {
   if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts) return NVMOE_ERR_INVALID_ARG;
-  if (T * k >= (int64_t(1) << 31)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (!slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (expert_offsets == nullptr || expert_counts == nullptr || ws == nullptr)
     return NVMOE_ERR_INVALID_ARG;
   if (T > 0 && (topk_ids == nullptr || row_token == nullptr || slot_of == nullptr))
@@ -193,8 +232,10 @@ int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
                        size_t ws_bytes, cudaStream_t stream) {
   if (rows < 0 || cols <= 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
   if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
-  if (cols % 64 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (cols % 64 != 0 || !elems_fit(rows, cols) || !elems_fit(out_rows, cols))
+    return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (fanout < 1 || fanout > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  if (row_dst != nullptr && !slots_fit(rows, fanout)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (row_dst == nullptr && (fanout != 1 || out_rows < rows)) return NVMOE_ERR_INVALID_ARG;
   if (gs_out == nullptr || ws == nullptr) return NVMOE_ERR_INVALID_ARG;
   if (rows > 0 && (x == nullptr || q == nullptr)) return NVMOE_ERR_INVALID_ARG;
@@ -284,7 +325,7 @@ static size_t forward_layout(int64_t T, int k, int E, int I, uint8_t* base, FwdB
 }
 
 size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I) {
-  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return 0;
+  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1 || !slots_fit(T, k)) return 0;
   FwdBuffers b;
   return forward_layout(T, k, E, I, nullptr, &b);
 }
@@ -314,7 +355,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
   const int E = w->E, H = w->H, I = w->I;
   if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;
-  if (H % 256 != 0 || I % 128 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 256 != 0 || I % 128 != 0 || !slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (w->w1 == nullptr || w->w1_sf == nullptr || w->gs_w1 == nullptr || w->w2 == nullptr ||
       w->w2_sf == nullptr || w->gs_w2 == nullptr || xq == nullptr || xsf_mma == nullptr ||
       gs_x == nullptr || expert_offsets == nullptr || expert_counts == nullptr ||
@@ -385,6 +426,13 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a1.partials = b.pieces;
   a1.counters = b.counters;
   a1.status = b.status;
+  if (taps != nullptr && taps->ready_flag != nullptr) {
+    a1.ready_flag = taps->ready_flag;
+    a1.ready_value = taps->ready_value;
+    a1.ready_limit_ns = taps->ready_wait_us > 0
+                            ? static_cast<uint64_t>(taps->ready_wait_us) * 1000u
+                            : 2000000000ull;
+  }
   GemmArgs a2{};
   a2.mode = 2;
   a2.E = E;
@@ -463,7 +511,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
 
 // ------------------------------------------------------------ router ----
 size_t moe_router_workspace_size(int64_t T, int H, int E) {
-  if (T < 0 || H < 1 || E < 1) return 0;
+  if (T < 0 || H < 1 || E < 1 || !elems_fit(T, H)) return 0;
   return router_workspace_bytes(T, H, E);
 }
 
@@ -474,7 +522,7 @@ int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E
     return NVMOE_ERR_INVALID_ARG;
   if (softmax_mode != NVMOE_ROUTER_SELECTED && softmax_mode != NVMOE_ROUTER_ALL)
     return NVMOE_ERR_INVALID_ARG;
-  if (H % 128 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 128 != 0 || !elems_fit(T, H) || !slots_fit(T, E)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return NVMOE_OK;
   if (x == nullptr || w_router == nullptr || topk_ids == nullptr || topk_w == nullptr ||
       ws == nullptr)
@@ -492,7 +540,7 @@ int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of, const fl
                          cudaStream_t stream) {
   if (T < 0 || k < 1 || k > kMaxTopK || H < 1) return NVMOE_ERR_INVALID_ARG;
   if (y_dtype != NVMOE_BF16 && y_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
-  if (H % 8 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 8 != 0 || !slots_fit(T, k) || !elems_fit(T, H)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return NVMOE_OK;
   if (slot_out == nullptr || slot_of == nullptr || topk_w == nullptr || y == nullptr)
     return NVMOE_ERR_INVALID_ARG;
@@ -544,7 +592,7 @@ static size_t layer_layout(int64_t T, int k, int E, int H, int I, uint8_t* base,
 }
 
 size_t moe_nvfp4_layer_workspace_size(int64_t T, int k, int E, int H, int I) {
-  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return 0;
+  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1 || !slots_fit(T, k)) return 0;
   LayerBuffers b;
   return layer_layout(T, k, E, H, I, nullptr, &b);
 }
@@ -558,7 +606,7 @@ int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
   if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;
   if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
   if (y_dtype != NVMOE_BF16 && y_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
-  if (H % 256 != 0 || I % 128 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 256 != 0 || I % 128 != 0 || !slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (ws == nullptr) return NVMOE_ERR_INVALID_ARG;
   if (T > 0 && (x == nullptr || topk_ids == nullptr || topk_w == nullptr || y == nullptr))
     return NVMOE_ERR_INVALID_ARG;
@@ -566,6 +614,7 @@ int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
   if (ws_bytes < moe_nvfp4_layer_workspace_size(T, k, E, H, I))
     return NVMOE_ERR_WORKSPACE_TOO_SMALL;
   const int path = taps != nullptr ? taps->path : NVMOE_PATH_AUTO;
+  if (taps != nullptr && taps->ready_flag != nullptr) return NVMOE_ERR_INVALID_ARG;
   if (T == 0) return NVMOE_OK;
   LayerBuffers b;
   layer_layout(T, k, E, H, I, static_cast<uint8_t*>(ws), &b);

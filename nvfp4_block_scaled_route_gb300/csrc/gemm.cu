@@ -19,19 +19,33 @@
 //                         loading L2 weights while the L1 tail and the
 //                         requantisation are still running.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (one CTA per SM):
 //   warp 0      TMA producer (A tile, two 128-row B tiles, staged scales)
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM)
-//               and tcgen05.mma
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (and, in the
+//               cooperative kernels, the tcgen05.cp scale copies)
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, one row per thread
 //               (and the requantisation in the fused kernel)
+//   warps 6..9  grouped_gemm_kernel only: scale writers, each stage's block
+//               scales from shared memory into TMEM with tcgen05.st, one
+//               warp per TMEM lane quarter.  tcgen05.cp copies of the scales
+//               run in the tensor pipe in series with the MMAs: at N = 256
+//               the 12 copies of a 256-K stage take 1.6x the time of its 4
+//               MMAs, and 5 wide (128x256b) copies 0.5x; stores from warps
+//               overlap the MMAs (98 % of the MMA-only rate, measured with
+//               the library's probe).  The cooperative decode kernels are
+//               bound by HBM, not the tensor pipe, and keep the copies and
+//               6 warps (more warps would cap their registers below what
+//               their epilogue and quantisation code use).
 //
 // Shared memory per stage (K = 256 elements = 128 bytes per row):
 //   A 128 rows x 128 B (16 KB), B 256 rows x 128 B (32 KB), both in the
 //   128-byte-swizzled K-major layout the TMA writes and the MMA reads;
 //   SFA 4 atoms (2 KB), SFB 2 x 4 atoms (4 KB) of 512-byte scale atoms.
-// TMEM (512 columns): accumulator in columns [0, 256); scale slots of
-// stage s at 256 + 48 s: SFA 4 columns per 64-element k-block, SFB 8.
+// TMEM (512 columns): accumulator in columns [0, 256); scale slot of
+// stage s at 256 + 64 s.  With scale writers: SFB in its first 32 columns
+// (8 per 64-element k-block), SFA in the next 16 (4 per k-block), every
+// tcgen05.st at a multiple of its column count.  With copies: SFA in the
+// first 16, SFB in the next 32.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -58,14 +72,17 @@ constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemBytes = kSmemUsed + 1024;            // alignment slack
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;                           // cooperative kernels
+constexpr int kThreadsSt = 320;                         // grouped_gemm_kernel
+constexpr int kSfWarp0 = 6;                             // first scale-writer warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
-constexpr uint32_t kTmemSfStage = 48;
+constexpr uint32_t kTmemSfStage = 64;
 
 struct __align__(8) Barriers {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t sf_full[kStages];       // the stage's scales are in TMEM (4 writer warps)
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -331,12 +348,14 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Bounded wait until *flag >= target.  Returns false on timeout (status set).
-__device__ bool wait_flag(const int* flag, int target, int* status, volatile int* abort) {
+// Bounded wait until *flag >= target.  Returns false on timeout (status set)
+// or when another role of the CTA has given up.
+__device__ bool wait_flag(const int* flag, int target, int* status, volatile int* abort,
+                          uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = globaltimer_ns();
   while (ld_acquire(flag) < target) {
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_status(status, kErrTimeout);
       if (abort != nullptr) *abort = 1;
       return false;
@@ -396,6 +415,11 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
   it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
   const uint64_t pol_a = policy_evict_last();
   const uint64_t pol_b = policy_evict_first();
+  // the caller's activation-ready flag: waited for before anything is
+  // loaded, so that a wait that runs out leaves no copy in flight
+  if (args.ready_flag != nullptr &&
+      !wait_flag(args.ready_flag, args.ready_value, args.status, abort, args.ready_limit_ns))
+    return false;
   bool gate_open = gate == nullptr;
   // activation loads waiting for the gate: (stage, a_row, ks, small box)
   int def_stage[kStages], def_row[kStages], def_ks[kStages];
@@ -494,6 +518,9 @@ __device__ void drain_producer(Barriers* bars, Pipe& pp, int* status) {
 }
 
 // ----------------------------------------------------------------- MMA --
+// kStSf: the stage's scales are written into TMEM by the writer warps
+// (wait for sf_full); else this thread copies them with tcgen05.cp.
+template <bool kStSf>
 __device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t tmem, Pipe& pp,
                         volatile int* abort) {
   const GemmArgs& args = *P.a;
@@ -506,20 +533,27 @@ __device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t 
     tc_fence_after();
     for (int ks = s0; ks < s1; ++ks) {
       if (!mbar_wait(&bars->full[pp.stage], pp.phase, args.status, abort)) return false;
+      if (kStSf && !mbar_wait(&bars->sf_full[pp.stage], pp.phase, args.status, abort))
+        return false;
       tc_fence_after();
       const int stage = pp.stage;
-      const uint32_t sfa_t = tmem + kTmemSf + stage * kTmemSfStage;
-      const uint32_t sfb_t = sfa_t + 16;
+      const uint32_t slot = tmem + kTmemSf + stage * kTmemSfStage;
+      const uint32_t sfa_t = kStSf ? slot + 32 : slot;
+      const uint32_t sfb_t = kStSf ? slot : slot + 16;
       const uint32_t a_base = smem_u32(smem + kOffA + stage * kABytes);
       const uint32_t b_base = smem_u32(smem + kOffB + stage * kBBytes);
-      const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
-      const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
       const int nkb = min(4, P.k_blocks - ks * 4);
-      for (int kb = 0; kb < nkb; ++kb) {
-        tmem_cp_32x128b_warpx4(sfa_t + kb * 4, smem_desc(sfa_s + kb * kSfAtomBytes, 16, 128, 0));
-        tmem_cp_32x128b_warpx4(sfb_t + kb * 8, smem_desc(sfb_s + kb * kSfAtomBytes, 16, 128, 0));
-        tmem_cp_32x128b_warpx4(sfb_t + kb * 8 + 4,
-                               smem_desc(sfb_s + kSfaBytes + kb * kSfAtomBytes, 16, 128, 0));
+      if (!kStSf) {
+        const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+        const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
+        for (int kb = 0; kb < nkb; ++kb) {
+          tmem_cp_32x128b_warpx4(sfa_t + kb * 4,
+                                 smem_desc(sfa_s + kb * kSfAtomBytes, 16, 128, 0));
+          tmem_cp_32x128b_warpx4(sfb_t + kb * 8,
+                                 smem_desc(sfb_s + kb * kSfAtomBytes, 16, 128, 0));
+          tmem_cp_32x128b_warpx4(sfb_t + kb * 8 + 4,
+                                 smem_desc(sfb_s + kSfaBytes + kb * kSfAtomBytes, 16, 128, 0));
+        }
       }
       for (int kb = 0; kb < nkb; ++kb) {
         const uint64_t adesc = smem_desc(a_base + kb * 32, 16, 1024, 2);
@@ -535,6 +569,60 @@ __device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t 
     }
     tc_commit(&bars->acc_full);
     pp.acc_phase ^= 1u;
+  }
+  return true;
+}
+
+// ------------------------------------------------------- scale writers --
+// Warps 6..9, one per TMEM lane quarter q = warp % 4.  For every stage of
+// this CTA's work (in the producer's order), once its loads have landed:
+// lane l reads the 16-byte row l of each 512-byte scale atom of the stage
+// (A: 4 atoms, one per k-block; B: 2 halves x 4 atoms) and writes them into
+// its own TMEM lane 32q + l.  Every quarter gets the same columns, the
+// layout the MMA reads: B k-block kb at slot + 8 kb + 4 h + j (half h,
+// column j = B row 128 h + 32 j + l), A k-block kb at slot + 32 + 4 kb + j
+// (column j = A row 32 j + l).  The slot is free once the stage's loads
+// have landed: the producer refills a stage only after the MMAs that read
+// its previous scales have completed.
+__device__ bool run_sf_writer(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t tmem,
+                              Pipe& pp, volatile int* abort) {
+  const GemmArgs& args = *P.a;
+  const int lane = threadIdx.x & 31;
+  const uint32_t q = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_base = tmem + ((q * 32u) << 16);
+  WorkIter it;
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  int tile, s0, s1;
+  while (it.next(tile, s0, s1)) {
+    for (int ks = s0; ks < s1; ++ks) {
+      if (!mbar_wait(&bars->full[pp.stage], pp.phase, args.status, abort)) return false;
+      const int stage = pp.stage;
+      const uint4* sa = reinterpret_cast<const uint4*>(smem + kOffSfa + stage * kSfaBytes) + lane;
+      const uint4* sb = reinterpret_cast<const uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane;
+      uint32_t a[16], b[32];
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint4 v = sa[kb * 32];                       // atom kb, row l
+        a[4 * kb] = v.x; a[4 * kb + 1] = v.y; a[4 * kb + 2] = v.z; a[4 * kb + 3] = v.w;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 u = sb[h * 128 + kb * 32];           // half h, atom kb, row l
+          b[8 * kb + 4 * h] = u.x; b[8 * kb + 4 * h + 1] = u.y;
+          b[8 * kb + 4 * h + 2] = u.z; b[8 * kb + 4 * h + 3] = u.w;
+        }
+      }
+      const uint32_t col = kTmemSf + stage * kTmemSfStage;
+      tmem_st_32x32b_x32(lane_base + col, b);
+      tmem_st_32x32b_x16(lane_base + col + 32, a);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->sf_full[stage]);
+      if (++pp.stage == kStages) {
+        pp.stage = 0;
+        pp.phase ^= 1u;
+      }
+    }
   }
   return true;
 }
@@ -858,6 +946,7 @@ __device__ uint32_t setup_cta(Barriers* bars, const CUtensorMap* m0, const CUten
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->sf_full[s], 4);
     }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 4);
@@ -901,7 +990,7 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 }
 
 // ------------------------------------------------------------- kernels --
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
+__global__ void __launch_bounds__(kThreadsSt, 1) grouped_gemm_kernel(
     const __grid_constant__ AMaps map_a, const __grid_constant__ CUtensorMap map_b,
     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -924,9 +1013,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      run_mma(P, bars, smem, tmem, pp, abort);
+      run_mma<true>(P, bars, smem, tmem, pp, abort);
       mma_drain(bars, args.status);
     }
+  } else if (warp >= kSfWarp0) {
+    run_sf_writer(P, bars, smem, tmem, pp, abort);
   } else {
     float amax = 0.0f;
     run_epilogue(P, __ldcg(args.gs_a), args.E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
@@ -1026,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
 #pragma unroll 1
       for (int ph = 0; ph < 2; ++ph) {
         const Phase P = ph ? P2 : P1;
-        if (!run_mma(P, bars, smem, tmem, pp, abort)) break;
+        if (!run_mma<false>(P, bars, smem, tmem, pp, abort)) break;
       }
       mma_drain(bars, a1.status);
     }
@@ -1332,7 +1423,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
 #pragma unroll 1
       for (int ph = 0; ph < 2; ++ph) {
         const Phase P = ph ? P2 : P1;
-        if (!run_mma(P, bars, smem, tmem, pp, abort)) break;
+        if (!run_mma<false>(P, bars, smem, tmem, pp, abort)) break;
       }
       mma_drain(bars, a1.status);
     }
@@ -1463,9 +1554,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   }
 }
 
-bool g_gemm_attr = false;
-bool g_fused_attr = false;
-bool g_layer_attr = false;
+PerDeviceOnce g_gemm_attr, g_fused_attr, g_layer_attr;
 
 }  // namespace
 
@@ -1473,12 +1562,10 @@ cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& ma
                          const CUtensorMap& map_w1, const AMaps& map_h,
                          const CUtensorMap& map_w2, const LayerLaunch& l, int grid,
                          cudaStream_t stream) {
-  if (!g_layer_attr) {
-    cudaError_t err = cudaFuncSetAttribute(layer_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBytes);
+  {
+    const cudaError_t err =
+        set_smem_attr_once(g_layer_attr, reinterpret_cast<const void*>(layer_kernel), kSmemBytes);
     if (err != cudaSuccess) return err;
-    g_layer_attr = true;
   }
   LayerArgs L{static_cast<const __nv_bfloat16*>(l.x), l.topk_ids, l.topk_w, l.T, l.k, l.rows,
               l.xq, l.xsf, l.gs_x, l.expert_offsets, l.expert_counts, l.row_token, l.slot_of,
@@ -1500,14 +1587,12 @@ int gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
                         int grid, cudaStream_t stream) {
-  if (!g_gemm_attr) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBytes);
+  {
+    const cudaError_t err =
+        set_smem_attr_once(g_gemm_attr, reinterpret_cast<const void*>(grouped_gemm_kernel), kSmemBytes);
     if (err != cudaSuccess) return err;
-    g_gemm_attr = true;
   }
-  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, args);
+  grouped_gemm_kernel<<<grid, kThreadsSt, kSmemBytes, stream>>>(map_a, map_b, args);
   return cudaGetLastError();
 }
 
@@ -1516,12 +1601,10 @@ cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps
                              const CUtensorMap& map_w2, int* grid_bar, const int32_t* row_token,
                              uint8_t* hq, uint8_t* hsf, float* gs_h, int grid,
                              cudaStream_t stream) {
-  if (!g_fused_attr) {
-    cudaError_t err = cudaFuncSetAttribute(fused_ffn_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBytes);
+  {
+    const cudaError_t err =
+        set_smem_attr_once(g_fused_attr, reinterpret_cast<const void*>(fused_ffn_kernel), kSmemBytes);
     if (err != cudaSuccess) return err;
-    g_fused_attr = true;
   }
   cudaError_t err = cudaMemsetAsync(grid_bar, 0, 2 * sizeof(int), stream);
   if (err != cudaSuccess) return err;

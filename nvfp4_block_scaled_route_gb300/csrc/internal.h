@@ -2,6 +2,7 @@
 // C-ABI layer (api.cu).  Not part of the public interface.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -9,12 +10,34 @@
 
 namespace nvmoe {
 
+// Kernel attributes (the dynamic shared-memory size) are set once per device
+// and kernel: one bit per device id (ids 0..63; larger ids set the attribute
+// on every launch).
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+};
+
+inline cudaError_t set_smem_attr_once(PerDeviceOnce& once, const void* fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (once.done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) once.done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 constexpr int kTileRows = 128;        // rows per tensor-core tile / SF atom row block
 constexpr int kSfAtomBytes = 512;     // 128 rows x 4 scale bytes
 constexpr int kStageK = 256;          // K elements per pipeline stage
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 constexpr int kQuantMaxPartials = 1024;
+
+// Adds to the count of kernels this library has enqueued
+// (nvmoe_kernel_launch_count).
+void note_launches(int kernels);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -88,6 +111,12 @@ struct GemmArgs {
   float* partials;        // split-tile pieces: [2 * grid][128][256] fp32
   int* counters;          // split-tile arrival counts: [kMaxSplitTiles], zero between calls
   int* status;
+  // Optional: the A operand (activation rows and their scales) is ready once
+  // *ready_flag >= ready_value; the producer waits for it (at most
+  // ready_limit_ns) before its first load.  nullptr = ready at launch.
+  const int* ready_flag;
+  int ready_value;
+  uint64_t ready_limit_ns;
 };
 constexpr int kMaxGrid = 256;
 constexpr int kMaxSplitTiles = 4 * kMaxGrid;
@@ -138,6 +167,15 @@ cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps
                              const CUtensorMap& map_w1, const AMaps& map_h,
                              const CUtensorMap& map_w2, int* grid_bar, const int32_t* row_token,
                              uint8_t* hq, uint8_t* hsf, float* gs_h, int grid,
+                             cudaStream_t stream);
+
+// ---- dense FP4 tensor-core probe (peak.cu) ----
+enum : int {
+  kProbePair = 1, kProbeN128 = 2, kProbeCp32 = 4, kProbeCp256 = 8,
+  kProbeAcc2 = 16, kProbeAcc4 = 32, kProbeNoAcc = 64, kProbeNoMma = 128,
+  kProbeCpAOnly = 256, kProbeCpEarly = 512, kProbeSt = 1024
+};
+cudaError_t launch_mma_probe(int variant, int iters, int grid, long long* cycles, int* status,
                              cudaStream_t stream);
 
 // ---- reduce ----

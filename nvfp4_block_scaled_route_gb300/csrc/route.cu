@@ -214,7 +214,8 @@ extern "C" int moe_route_permute_noalloc(const int32_t* topk_ids, int64_t T, int
                                          cudaStream_t stream) {
   using namespace nvmoe;
   if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts) return NVMOE_ERR_INVALID_ARG;
-  if (T * k >= (int64_t(1) << 31)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  // T*k < 2^31, tested without forming the product (T may be any int64)
+  if (T > int64_t{INT32_MAX} / k) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (expert_offsets == nullptr || expert_counts == nullptr) return NVMOE_ERR_INVALID_ARG;
   if (T > 0 && (topk_ids == nullptr || row_token == nullptr || slot_of == nullptr))
     return NVMOE_ERR_INVALID_ARG;
@@ -231,5 +232,7 @@ extern "C" int moe_route_permute_noalloc(const int32_t* topk_ids, int64_t T, int
   const cudaError_t e = launch_route(topk_ids, T, k, E, expert_offsets, expert_counts, row_token,
                                      rows, slot_of, counts, static_cast<int>(n_chunks), nullptr,
                                      stream);
-  return e == cudaSuccess ? NVMOE_OK : NVMOE_ERR_CUDA;
+  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  note_launches(n_chunks == 1 ? 1 : 2);
+  return NVMOE_OK;
 }

@@ -69,6 +69,10 @@ CONFIGS = {
     "prefill16k": MoEConfig("prefill16k", E=48, H=7168, I=3072, T=16384, k=8,
                             routing="hot_expert", act="student_t"),
     # parity-sized cases (not benchmark workloads)
+    # the largest batch the single-kernel layer path takes at these sizes
+    # (T*k = 16 slots: at most 16 m-tiles x 28 L2 n-tiles below 4 per SM)
+    "decode2": MoEConfig("decode2", E=48, H=7168, I=3072, T=2, k=8,
+                         routing="uniform"),
     "small": MoEConfig("small", E=6, H=512, I=256, T=97, k=3, routing="zipf"),
     "medium": MoEConfig("medium", E=8, H=1024, I=768, T=600, k=4,
                         routing="zipf"),

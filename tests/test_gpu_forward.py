@@ -21,12 +21,10 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe as omoe
-from oracle import nvfp4 as onv
+from oracle.cpp import moe as omoe, nvfp4 as onv
 from nvfp4_block_scaled_route_gb300 import synthetic as syn
 
 from _layout import unstage
-import _oracle_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -246,11 +244,13 @@ def test_forward_decode_full_size(nb):
     used = sorted(set(ids.flatten().tolist()))
     W1 = torch.stack([syn.draw_weight(cfg, 1, e, device=DEV) for e in range(cfg.E)])
     W2 = torch.stack([syn.draw_weight(cfg, 2, e, device=DEV) for e in range(cfg.E)])
-    args = [(W1[e].cpu().numpy(), W2[e].cpu().numpy()) for e in used]
+    qs = {}
+    for e in used:
+        q1, s1, g1 = onv.quantize_weight(W1[e].cpu().numpy())
+        q2, s2, g2 = onv.quantize_weight(W2[e].cpu().numpy())
+        qs[e] = (q1, s1, g1, q2, s2, g2)
     g = run_gpu(nb, cfg, x, ids, w, W1, W2)
     del W1, W2
-    with _oracle_pool.pool(len(used)) as p:
-        qs = dict(zip(used, p.map(_oracle_pool.quantize_pair, args)))
     for e in used:
         assert float(qs[e][2]) == float(g["gs_w1"][e])
         assert float(qs[e][5]) == float(g["gs_w2"][e])

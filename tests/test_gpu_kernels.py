@@ -9,8 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe as omoe
-from oracle import nvfp4 as onv
+from oracle.cpp import moe as omoe, nvfp4 as onv
 from nvfp4_block_scaled_route_gb300 import synthetic as syn
 
 from _layout import stage, unstage
@@ -274,6 +273,7 @@ def _l1_only(nb, xq_rows, xsf_rows, w1q, w1sf, gs_x=1.0, gs_w=None):
     # L2 weights: zeros (their output is not inspected here)
     w2q = torch.zeros((E, I // 2, H), dtype=torch.uint8)
     w2sf = torch.full((E, I // 16, H), 0x38, dtype=torch.uint8)
+    w1q, w1sf = np.ascontiguousarray(w1q), np.ascontiguousarray(w1sf)
     pw = nb.PreparedWeights.from_checkpoint(torch.from_numpy(w1q).to(DEV),
                                             torch.from_numpy(w1sf).to(DEV), gs1.to(DEV),
                                             w2q.to(DEV), w2sf.to(DEV), gs1.to(DEV))

@@ -1,6 +1,8 @@
 """Pins of the CPU oracle against what the pages and the mathematics fix.
 
-Each test ties one oracle function to something other than itself: values
+Each test runs against both oracles, the plain C++ one (oracle/
+nvfp4_oracle.cpp, the oracle of record) and the numpy one, and ties one
+oracle function to something other than itself: values
 the pages print (tests/golden/, each file citing its passage), closed forms,
 a library routine for a special case (torch's float8_e4m3fn view and cast),
 or pure-Python brute force on tiny inputs with a different loop structure.
@@ -16,8 +18,24 @@ import pytest
 import torch
 
 from oracle import moe, nvfp4
+from oracle import cpp as _cpp
+from oracle import moe as _np_moe, nvfp4 as _np_nvfp4
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True, params=["cpp", "numpy"])
+def backend(request):
+    """Every pin runs against both oracles: the plain C++ one (the oracle of
+    record) and the numpy one (its cross-check).  The pins name the two
+    modules ``nvfp4`` and ``moe``; this rebinds them for each pass."""
+    global nvfp4, moe
+    if request.param == "cpp":
+        nvfp4, moe = _cpp.nvfp4, _cpp.moe
+    else:
+        nvfp4, moe = _np_nvfp4, _np_moe
+    yield request.param
+    nvfp4, moe = _np_nvfp4, _np_moe
 
 
 def golden_rows(name):
