@@ -70,11 +70,13 @@ typedef enum {
   NVMOE_ERR_WORKSPACE_TOO_SMALL = 4,
   NVMOE_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed     */
   NVMOE_ERR_TIMEOUT = 6,            /* device: a bounded wait ran out        */
-  NVMOE_ERR_DEVICE_BAD_INDEX = 7    /* device: expert id out of [0, E)       */
+  NVMOE_ERR_DEVICE_BAD_INDEX = 7,   /* device: expert id out of [0, E)       */
+  NVMOE_ERR_RANGE = 8               /* device: a value exceeded the range of
+                                       its storage type (fp16 slot rows)     */
 } nvmoe_status;
 
 /* Element types of activation / output buffers. */
-typedef enum { NVMOE_BF16 = 0, NVMOE_F32 = 1 } nvmoe_dtype;
+typedef enum { NVMOE_BF16 = 0, NVMOE_F32 = 1, NVMOE_F16 = 2 } nvmoe_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvmoe_status_str(int status);
@@ -341,7 +343,13 @@ typedef struct {
  *   xsf_mma   staged scales of xq: nvfp4_sf_mma_bytes(rows, H)
  *   gs_x      float [1]
  *   expert_offsets, expert_counts, row_token: from moe_route_permute
- *   slot_out  float [rows, H]  (padding rows unspecified)
+ *   slot_out  [rows, H] of slot_out_dtype: NVMOE_F32, NVMOE_F16 or NVMOE_BF16
+ *             (the fp32 alpha-scaled result rounded to nearest even: half the
+ *             bytes written here and read by the reduce; fp16 is within
+ *             2^-11 relative, bf16 within 2^-8).  With fp16 a value of
+ *             magnitude above 65504 records NVMOE_ERR_RANGE in the status
+ *             word (the stored value is then inf).
+ *             (padding rows unspecified)
  * rows = moe_route_rows_bound(T, k, E).
  * Workspace: moe_nvfp4_workspace_size bytes, zero-filled before its first
  * use; the call leaves it ready for the next call (split-tile counters are
@@ -358,7 +366,7 @@ int moe_nvfp4_forward(const nvmoe_weights* weights, const uint8_t* xq,
                       const uint8_t* xsf_mma, const float* gs_x,
                       const int32_t* expert_offsets, const int32_t* expert_counts,
                       const int32_t* row_token, int64_t T, int k,
-                      float* slot_out, const nvmoe_taps* taps,
+                      void* slot_out, int slot_out_dtype, const nvmoe_taps* taps,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------- router front end --
@@ -391,13 +399,15 @@ int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E
  *   y[t, :] = sum_{j = 0..k-1} topk_w[t, j] * slot_out[slot_of[t*k + j], :]
  * accumulated in fp32 in ascending j, stored once as y_dtype (bf16 rounds to
  * nearest even).
- *   slot_out float [rows, H];  slot_of int32 [T*k];  topk_w float [T, k]
+ *   slot_out [rows, H] of slot_out_dtype (NVMOE_F32, NVMOE_F16 or
+ *            NVMOE_BF16; both 16-bit types widen exactly);  slot_of int32
+ *            [T*k];  topk_w float [T, k]
  *   y        [T, H] of y_dtype (NVMOE_BF16 or NVMOE_F32)
  * Limits: H % 8 == 0, 1 <= k <= 32.
  */
-int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of,
-                         const float* topk_w, int64_t T, int k, int64_t H,
-                         void* y, int y_dtype, cudaStream_t stream);
+int moe_unpermute_reduce(const void* slot_out, int slot_out_dtype,
+                         const int32_t* slot_of, const float* topk_w, int64_t T, int k,
+                         int64_t H, void* y, int y_dtype, cudaStream_t stream);
 
 /* ----------------------------------------------------------- steps 1-7 --
  * moe_nvfp4_layer_forward — the whole layer in one call: the four steps
@@ -418,6 +428,9 @@ int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of,
  * select the paths of moe_nvfp4_forward after separate routing and
  * quantisation launches.  taps->slot_of, when given, receives the slot row
  * of every (token, choice).
+ * Above the single-kernel limits the slot rows between the L2 GEMM and the
+ * reduce are held in fp16 (see moe_nvfp4_forward: NVMOE_ERR_RANGE reports a
+ * value beyond its range).
  * Workspace: moe_nvfp4_layer_workspace_size bytes, zero-filled before first
  * use; its status word (nvmoe_read_status) is the forward's.  The kernel
  * leaves its barrier words and reduce counters at zero for the next call;

@@ -17,7 +17,7 @@ import torch
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libnvfp4moe.so")
 
-BF16, F32 = 0, 1
+BF16, F32, F16 = 0, 1, 2
 TILE_ROWS = 128
 
 _lib = None
@@ -70,8 +70,8 @@ SIGNATURES = {
     "moe_nvfp4_prepare_weights": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_nvfp4_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_nvfp4_forward": (_I, [ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _I64, _I, _P,
-                               ctypes.POINTER(Taps), _P, _SZ, _P]),
-    "moe_unpermute_reduce": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _I, _P]),
+                               _I, ctypes.POINTER(Taps), _P, _SZ, _P]),
+    "moe_unpermute_reduce": (_I, [_P, _I, _P, _P, _I64, _I, _I64, _P, _I, _P]),
     "moe_router_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_router_topk": (_I, [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_nvfp4_layer_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
@@ -358,10 +358,12 @@ def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Ten
                                                 weights.I), dev)
     t = _taps(taps)
     wst = weights.struct()
+    code = {torch.bfloat16: BF16, torch.float32: F32, torch.float16: F16}[slot_out.dtype]
     _check("moe_nvfp4_forward", lib().moe_nvfp4_forward(
         ctypes.byref(wst), _ptr(xq), _ptr(xsf_mma), _ptr(gs_x), _ptr(route.expert_offsets),
         _ptr(route.expert_counts), _ptr(route.row_token), route.T, route.k, _ptr(slot_out),
-        ctypes.byref(t) if t is not None else None, _ptr(ws), ws.numel(), _stream(stream)))
+        code, ctypes.byref(t) if t is not None else None, _ptr(ws), ws.numel(),
+        _stream(stream)))
     return slot_out
 
 
@@ -373,8 +375,10 @@ def unpermute_reduce(slot_out: torch.Tensor, slot_of: torch.Tensor, topk_w: torc
     if y is None:
         y = torch.empty((T, H), dtype=out_dtype, device=slot_out.device)
     code = {torch.bfloat16: BF16, torch.float32: F32}[y.dtype]
+    scode = {torch.bfloat16: BF16, torch.float32: F32, torch.float16: F16}[slot_out.dtype]
     _check("moe_unpermute_reduce", lib().moe_unpermute_reduce(
-        _ptr(slot_out), _ptr(slot_of), _ptr(topk_w), T, k, H, _ptr(y), code, _stream(stream)))
+        _ptr(slot_out), scode, _ptr(slot_of), _ptr(topk_w), T, k, H, _ptr(y), code,
+        _stream(stream)))
     return y
 
 
@@ -389,7 +393,7 @@ class MoELayer:
     """
 
     def __init__(self, weights: PreparedWeights, T: int, k: int, device="cuda",
-                 out_dtype=torch.bfloat16):
+                 out_dtype=torch.bfloat16, slot_dtype=torch.float32):
         self.w = weights
         self.T, self.k = T, k
         E, H, I = weights.E, weights.H, weights.I
@@ -406,7 +410,7 @@ class MoELayer:
         self.xq = torch.zeros((max(self.rows, 1), H // 2), dtype=torch.uint8, device=dev)
         self.xsf = torch.zeros(max(sf_mma_bytes(self.rows, H), 16), dtype=torch.uint8, device=dev)
         self.gs_x = torch.zeros(1, dtype=torch.float32, device=dev)
-        self.slot_out = torch.zeros((max(self.rows, 1), H), dtype=torch.float32, device=dev)
+        self.slot_out = torch.zeros((max(self.rows, 1), H), dtype=slot_dtype, device=dev)
         self.y = torch.empty((T, H), dtype=out_dtype, device=dev)
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,

@@ -134,6 +134,7 @@ const char* nvmoe_status_str(int s) {
     case NVMOE_ERR_CUDA: return "CUDA error";
     case NVMOE_ERR_TIMEOUT: return "device wait timed out";
     case NVMOE_ERR_DEVICE_BAD_INDEX: return "expert id out of range";
+    case NVMOE_ERR_RANGE: return "value beyond the range of its storage type";
     default: return "unknown status";
   }
 }
@@ -334,25 +335,29 @@ size_t moe_nvfp4_workspace_size(int64_t T, int k, int E, int H, int I) {
 static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
                         const float* gs_x, const int32_t* expert_offsets,
                         const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
-                        float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
-                        cudaStream_t stream, LayerLaunch* layer);
+                        void* slot_out, int slot_out_dtype, const nvmoe_taps* taps, void* ws,
+                        size_t ws_bytes, cudaStream_t stream, LayerLaunch* layer);
 
 int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
                       const float* gs_x, const int32_t* expert_offsets,
                       const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
-                      float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
-                      cudaStream_t stream) {
+                      void* slot_out, int slot_out_dtype, const nvmoe_taps* taps, void* ws,
+                      size_t ws_bytes, cudaStream_t stream) {
   if (taps != nullptr && taps->path == NVMOE_PATH_LAYER) return NVMOE_ERR_INVALID_ARG;
   return forward_impl(w, xq, xsf_mma, gs_x, expert_offsets, expert_counts, row_token, T, k,
-                      slot_out, taps, ws, ws_bytes, stream, nullptr);
+                      slot_out, slot_out_dtype, taps, ws, ws_bytes, stream, nullptr);
 }
 
 static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
                         const float* gs_x, const int32_t* expert_offsets,
                         const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
-                        float* slot_out, const nvmoe_taps* taps, void* ws, size_t ws_bytes,
-                        cudaStream_t stream, LayerLaunch* layer) {
+                        void* slot_out, int slot_out_dtype, const nvmoe_taps* taps, void* ws,
+                        size_t ws_bytes, cudaStream_t stream, LayerLaunch* layer) {
   if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  if (slot_out_dtype != NVMOE_BF16 && slot_out_dtype != NVMOE_F32 && slot_out_dtype != NVMOE_F16)
+    return NVMOE_ERR_INVALID_ARG;
+  // the single-kernel layer path reduces from fp32 slot rows inside the kernel
+  if (layer != nullptr && slot_out_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
   const int E = w->E, H = w->H, I = w->I;
   if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;
   if (H % 256 != 0 || I % 128 != 0 || !slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
@@ -421,6 +426,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   // the layer kernel requantises after its grid barrier, spread over the grid
   a1.mid_in_epilogue = layer == nullptr;
   a1.out = b.h;
+  a1.out_dtype = NVMOE_F32;
   a1.tap = tap_l1;
   a1.amax_partial = b.amax;
   a1.partials = b.pieces;
@@ -447,7 +453,8 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a2.gs_a = b.gs_h;
   a2.gs_b = w->gs_w2;
   a2.gs_mid = w->gs_mid;
-  a2.out = slot_out;
+  a2.out = static_cast<float*>(slot_out);
+  a2.out_dtype = slot_out_dtype;
   a2.tap = nullptr;
   a2.amax_partial = nullptr;
   a2.partials = b.pieces;
@@ -535,17 +542,20 @@ int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E
 }
 
 // ------------------------------------------------------------ reduce ----
-int moe_unpermute_reduce(const float* slot_out, const int32_t* slot_of, const float* topk_w,
-                         int64_t T, int k, int64_t H, void* y, int y_dtype,
+int moe_unpermute_reduce(const void* slot_out, int slot_out_dtype, const int32_t* slot_of,
+                         const float* topk_w, int64_t T, int k, int64_t H, void* y, int y_dtype,
                          cudaStream_t stream) {
   if (T < 0 || k < 1 || k > kMaxTopK || H < 1) return NVMOE_ERR_INVALID_ARG;
   if (y_dtype != NVMOE_BF16 && y_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (slot_out_dtype != NVMOE_BF16 && slot_out_dtype != NVMOE_F32 && slot_out_dtype != NVMOE_F16)
+    return NVMOE_ERR_INVALID_ARG;
   if (H % 8 != 0 || !slots_fit(T, k) || !elems_fit(T, H)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return NVMOE_OK;
   if (slot_out == nullptr || slot_of == nullptr || topk_w == nullptr || y == nullptr)
     return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(slot_out) || !aligned16(y)) return NVMOE_ERR_MISALIGNED;
-  return status_of(counted(launch_reduce(slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream), 1));
+  return status_of(counted(launch_reduce(slot_out, slot_out_dtype, slot_of, topk_w, T, k, H, y,
+                                         y_dtype, stream), 1));
 }
 
 // ------------------------------------------------------------- layer ----
@@ -563,7 +573,7 @@ struct LayerBuffers {
   float* gs_x;
   uint8_t* quant_ws;
   size_t quant_ws_bytes;
-  float* slot_out;
+  void* slot_out;          // fp32 (single-kernel path) or bf16 rows
   int* grid_bar;
   int* ycnt;
 };
@@ -585,7 +595,7 @@ static size_t layer_layout(int64_t T, int k, int E, int H, int I, uint8_t* base,
   b->gs_x = c.take<float>(sizeof(float));
   b->quant_ws_bytes = nvfp4_quantize_workspace_size(T, H);
   b->quant_ws = c.take<uint8_t>(b->quant_ws_bytes);
-  b->slot_out = c.take<float>(static_cast<size_t>(rows) * H * sizeof(float));
+  b->slot_out = c.take<uint8_t>(static_cast<size_t>(rows) * H * sizeof(float));
   b->grid_bar = c.take<int>(kLayerBarWords * sizeof(int));
   b->ycnt = c.take<int>(static_cast<size_t>(T > 0 ? T : 1) * (H / 256 + 1) * sizeof(int));
   return c.off;
@@ -649,7 +659,7 @@ int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
     l.y = y;
     l.y_dtype = y_dtype;
     return forward_impl(w, b.xq, b.xsf, b.gs_x, b.offsets, b.counts, b.row_token, T, k,
-                        b.slot_out, taps, b.fwd_ws, b.fwd_ws_bytes, stream, &l);
+                        b.slot_out, NVMOE_F32, taps, b.fwd_ws, b.fwd_ws_bytes, stream, &l);
   }
   int st = moe_route_permute(topk_ids, T, k, E, b.offsets, b.counts, b.row_token, slot_of,
                              b.route_ws, b.route_ws_bytes, stream);
@@ -657,10 +667,15 @@ int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
   st = nvfp4_quantize_act(x, x_dtype, T, H, slot_of, k, rows, b.xq, nullptr, b.xsf, b.gs_x,
                           b.quant_ws, b.quant_ws_bytes, stream);
   if (st != NVMOE_OK) return st;
+  // slot rows in fp16: half the bytes of the L2 epilogue's stores and of the
+  // reduce's loads; the rounding (at most 2^-11 relative) stays well inside
+  // the 2e-3 * row-amax tolerance of a GEMM output, and a value beyond the
+  // fp16 range is reported (NVMOE_ERR_RANGE), never clamped
   st = forward_impl(w, b.xq, b.xsf, b.gs_x, b.offsets, b.counts, b.row_token, T, k, b.slot_out,
-                    taps, b.fwd_ws, b.fwd_ws_bytes, stream, nullptr);
+                    NVMOE_F16, taps, b.fwd_ws, b.fwd_ws_bytes, stream, nullptr);
   if (st != NVMOE_OK) return st;
-  return moe_unpermute_reduce(b.slot_out, slot_of, topk_w, T, k, H, y, y_dtype, stream);
+  return moe_unpermute_reduce(b.slot_out, NVMOE_F16, slot_of, topk_w, T, k, H, y, y_dtype,
+                              stream);
 }
 
 }  // extern "C"

@@ -47,6 +47,7 @@
 // tcgen05.st at a multiple of its column count.  With copies: SFA in the
 // first 16, SFB in the next 32.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -241,9 +242,44 @@ __device__ __forceinline__ void epi_l1(const float (&g)[32], const float (&u)[32
   }
 }
 
-// L2 epilogue on 32 columns.
+// Two values as one bf16x2 word (round to nearest even), first in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Two values as one fp16x2 word (round to nearest even), first in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// fp16 holds magnitudes up to 65504: a larger slot value is reported on the
+// device (NVMOE_ERR_RANGE), never silently clamped.
+constexpr float kF16Max = 65504.0f;
+
+// L2 epilogue on 32 columns: slot_out = alpha * acc, stored as fp32, bf16 or
+// fp16 (args.out_dtype 1, 0, 2).
 __device__ __forceinline__ void epi_l2(const float (&a)[32], float alpha, int64_t row, int col,
                                        const GemmArgs& args) {
+  if (args.out_dtype != 1) {
+    const bool half = args.out_dtype == 2;
+    uint16_t* op = reinterpret_cast<uint16_t*>(args.out) + row * args.N + col;
+    float big = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; i += 16) {
+      float w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float lo = __fmul_rn(alpha, a[i + 2 * j]), hi = __fmul_rn(alpha, a[i + 2 * j + 1]);
+        big = fmaxf(big, fmaxf(fabsf(lo), fabsf(hi)));
+        w[j] = __uint_as_float(half ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi));
+      }
+      st_global_v8(reinterpret_cast<float*>(op + i), w);
+    }
+    if (half && !(big <= kF16Max)) record_status(args.status, kErrRange);
+    return;
+  }
   float* op = args.out + row * args.N + col;
 #pragma unroll
   for (int i = 0; i < 32; i += 8) {
@@ -280,6 +316,19 @@ __device__ __forceinline__ void epi_l1_4(float4 g, float4 u, float alpha, float 
 
 __device__ __forceinline__ void epi_l2_4(float4 a, float alpha, int64_t row, int col,
                                          const GemmArgs& args) {
+  if (args.out_dtype != 1) {
+    uint16_t* op = reinterpret_cast<uint16_t*>(args.out) + row * args.N + col;
+    const float v[4] = {__fmul_rn(alpha, a.x), __fmul_rn(alpha, a.y), __fmul_rn(alpha, a.z),
+                        __fmul_rn(alpha, a.w)};
+    if (args.out_dtype == 2) {
+      *reinterpret_cast<uint2*>(op) = make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
+      const float big = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      if (!(big <= kF16Max)) record_status(args.status, kErrRange);
+    } else {
+      *reinterpret_cast<uint2*>(op) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+    }
+    return;
+  }
   *reinterpret_cast<float4*>(args.out + row * args.N + col) =
       make_float4(__fmul_rn(alpha, a.x), __fmul_rn(alpha, a.y), __fmul_rn(alpha, a.z),
                   __fmul_rn(alpha, a.w));

@@ -106,6 +106,7 @@ struct GemmArgs {
   bool mid_in_epilogue;   // L1 with gs_mid: requantise in the epilogue (else the
                           // caller requantises after its grid barrier)
   float* out;             // L1: h [rows, I]; L2: slot_out [rows, N]
+  int out_dtype;          // L2: slot_out element type, 0 bf16, 1 fp32, 2 fp16 (RNE)
   float* tap;             // L1: l1_out [rows, 2I] or null
   float* amax_partial;    // L1: [grid]
   float* partials;        // split-tile pieces: [2 * grid][128][256] fp32
@@ -185,8 +186,8 @@ size_t router_workspace_bytes(int64_t T, int H, int E);
 cudaError_t launch_router(const void* x, const void* w, int64_t T, int H, int E, int k, int mode,
                           int32_t* ids, float* weights, float* partials, cudaStream_t stream);
 
-cudaError_t launch_reduce(const float* slot_out, const int32_t* slot_of, const float* topk_w,
-                          int64_t T, int k, int64_t H, void* y, int y_dtype,
+cudaError_t launch_reduce(const void* slot_out, int slot_dtype, const int32_t* slot_of,
+                          const float* topk_w, int64_t T, int k, int64_t H, void* y, int y_dtype,
                           cudaStream_t stream);
 
 }  // namespace nvmoe

@@ -16,6 +16,7 @@ enum : int {
   kOk = 0,
   kErrTimeout = 6,
   kErrBadIndex = 7,
+  kErrRange = 8,
 };
 
 // Upper bound on any single wait inside a kernel (nanoseconds of

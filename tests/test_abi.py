@@ -85,10 +85,15 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     from nvfp4_block_scaled_route_gb300 import binding
     w = binding.Weights(4, 320, 128, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)
     assert lib.moe_nvfp4_forward(ctypes.byref(w), fake, fake, fake, fake, fake, fake, 1, 2,
-                                 fake, None, fake, 1 << 30, None) == 2
+                                 fake, 1, None, fake, 1 << 30, None) == 2
+    # slot_out dtype other than bf16 / fp32
+    w.H = 256
+    assert lib.moe_nvfp4_forward(ctypes.byref(w), fake, fake, fake, fake, fake, fake, 1, 2,
+                                 fake, 7, None, fake, 1 << 30, None) == 1
     # reduce: bad dtype, bad H
-    assert lib.moe_unpermute_reduce(fake, fake, fake, 2, 2, 64, fake, 5, None) == 1
-    assert lib.moe_unpermute_reduce(fake, fake, fake, 2, 2, 60, fake, 0, None) == 2
+    assert lib.moe_unpermute_reduce(fake, 1, fake, fake, 2, 2, 64, fake, 5, None) == 1
+    assert lib.moe_unpermute_reduce(fake, 3, fake, fake, 2, 2, 64, fake, 0, None) == 1
+    assert lib.moe_unpermute_reduce(fake, 0, fake, fake, 2, 2, 60, fake, 0, None) == 2
 
 
 def test_router_and_layer_arguments_are_rejected_on_the_host(lib):

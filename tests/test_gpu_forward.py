@@ -115,11 +115,12 @@ def flip_adjusted(ref, hq_g, hsf_g, w2, topk_w):
     return out2, y64
 
 
-def run_gpu(nb, cfg, x, ids, w, W1_dev, W2_dev, out_dtype=torch.float32, path=0):
+def run_gpu(nb, cfg, x, ids, w, W1_dev, W2_dev, out_dtype=torch.float32, path=0,
+            slot_dtype=torch.float32):
     q1, s1, g1 = nb.quantize_weights(W1_dev)
     q2, s2, g2 = nb.quantize_weights(W2_dev)
     pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
-    layer = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=out_dtype)
+    layer = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=out_dtype, slot_dtype=slot_dtype)
     rows = layer.rows
     taps = dict(l1_out=torch.zeros((rows, 2 * cfg.I), dtype=torch.float32, device=DEV),
                 h=torch.zeros((rows, cfg.I), dtype=torch.float32, device=DEV),
@@ -347,7 +348,8 @@ def test_layer_kernel_equals_four_calls(nb, cfg, out_dtype):
 
 
 def test_layer_forward_large_batch_uses_four_launches(nb):
-    """Above the single-kernel limits the one-call API runs the four steps."""
+    """Above the single-kernel limits the one-call API runs the four steps
+    (with fp16 slot rows): the same bits as the four calls made directly."""
     cfg = syn.CONFIGS["small"]                       # T*k = 291 > 128
     x = syn.draw_activations(cfg)
     ids, w = syn.draw_routing(cfg)
@@ -356,7 +358,7 @@ def test_layer_forward_large_batch_uses_four_launches(nb):
     with pytest.raises(nb.NvmoeError):
         run_gpu_layer(nb, cfg, x, ids, w, W1, W2, path=3)
     a = run_gpu_layer(nb, cfg, x, ids, w, W1, W2, path=0)
-    b = run_gpu(nb, cfg, x, ids, w, W1, W2, path=0)
+    b = run_gpu(nb, cfg, x, ids, w, W1, W2, path=0, slot_dtype=torch.float16)
     assert np.array_equal(a["y"], b["y"])
 
 
@@ -490,3 +492,74 @@ def test_forward_static_mid_scale(nb, name, path):
     if sum(flips):
         _, y64 = flip_adjusted(ref, hq_g, hsf_g, w2q, w.numpy())
     rows_close(y.cpu().numpy(), y64, "y")
+
+
+# ------------------------------------------------- 16-bit slot rows ----
+
+@pytest.mark.parametrize("slot_dtype,rel", [(torch.float16, 2.0 ** -11), (torch.bfloat16, 2.0 ** -8)],
+                         ids=["f16", "bf16"])
+@pytest.mark.parametrize("name,path", [("small", 1), ("medium", 2), ("waves", 1)])
+def test_forward_16bit_slot_rows(nb, name, path, slot_dtype, rel):
+    """slot_out held in fp16 or bf16 (the fp32 alpha-scaled L2 result rounded
+    to nearest even).  Each slot value is within the GEMM bound plus its own
+    rounding (rel * |v|; fp16's 2^-11 stays inside 2e-3 * row-amax), and y
+    (fp32) within the GEMM bound plus the rounding carried through the
+    weighted sum (rel * sum_j w_j |slot_j|)."""
+    cfg = syn.CONFIGS[name]
+    x = syn.draw_activations(cfg)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)])
+    q1, s1, g1 = nb.quantize_weights(W1.to(DEV))
+    q2, s2, g2 = nb.quantize_weights(W2.to(DEV))
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    layer = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=torch.float32,
+                        slot_dtype=slot_dtype)
+    rows = layer.rows
+    taps = dict(hq=torch.zeros((rows, cfg.I // 2), dtype=torch.uint8, device=DEV),
+                hsf_mma=torch.zeros(nb.sf_mma_bytes(rows, cfg.I), dtype=torch.uint8, device=DEV),
+                path=path)
+    y = layer.forward(x.to(DEV), ids.to(DEV), w.to(DEV), taps=taps)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    w2q = omoe.quantize_expert_weights(list(W2.numpy()))
+    ref = omoe.forward(x.float().numpy(), ids.numpy(), w.numpy(),
+                       *omoe.quantize_expert_weights(list(W1.numpy())), *w2q)
+    r = ref["route"]
+    dense_rows = np.empty(cfg.T * cfg.k, dtype=np.int64)
+    dense_rows[r["slot_of"]] = layer.route.slot_of.cpu().numpy()[:cfg.T * cfg.k]
+    hq_g = taps["hq"].cpu().numpy()[dense_rows]
+    hsf_g = unstage(taps["hsf_mma"].cpu().numpy(), rows, cfg.I)[dense_rows]
+    flips = check_requant(ref["h"], ref["gs_h"], ref["hq"], ref["hsf"], hq_g, hsf_g)
+    out2, y64 = ref["out2"], ref["y64"]
+    if sum(flips):
+        out2, y64 = flip_adjusted(ref, hq_g, hsf_g, w2q, w.numpy())
+    so = layer.slot_out.double().cpu().numpy()[dense_rows]
+    bound = GEMM_TOL * np.abs(out2).max(1, keepdims=True) + rel * np.abs(out2)
+    assert np.all(np.abs(so - out2) <= bound)
+    if slot_dtype == torch.float16:
+        rows_close(so, out2, "slot_out")          # the GEMM bar itself holds
+    carried = rel * omoe.unpermute_reduce(np.abs(out2), r["slot_of"], np.abs(w.numpy()))
+    yb = GEMM_TOL * np.abs(y64).max(1, keepdims=True) + carried
+    assert np.all(np.abs(y.double().cpu().numpy() - y64) <= yb)
+
+
+def test_fp16_slot_rows_report_overflow(nb):
+    """A slot value beyond the fp16 range is reported (NVMOE_ERR_RANGE = 8),
+    not clamped; fp32 slot rows of the same input report nothing."""
+    cfg = syn.CONFIGS["small"]
+    x = (syn.draw_activations(cfg).float() * 3.0e4).to(torch.bfloat16)
+    ids, w = syn.draw_routing(cfg)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)])
+    q1, s1, g1 = nb.quantize_weights(W1.to(DEV))
+    q2, s2, g2 = nb.quantize_weights(W2.to(DEV))
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    for dt, want in ((torch.float16, 8), (torch.float32, 0)):
+        layer = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=torch.float32, slot_dtype=dt)
+        layer.forward(x.to(DEV), ids.to(DEV), w.to(DEV))
+        torch.cuda.synchronize()
+        assert layer.status() == want
+        if dt == torch.float32:
+            assert float(layer.slot_out.abs().max()) > 65504.0
+

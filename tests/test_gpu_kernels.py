@@ -348,16 +348,20 @@ def test_gemm_single_scale_probe(nb, m, g):
 
 # ---------------------------------------------------------------- reduce --
 
+@pytest.mark.parametrize("slot_dtype", [torch.float32, torch.float16, torch.bfloat16],
+                         ids=["slot_f32", "slot_f16", "slot_bf16"])
 @pytest.mark.parametrize("T,k,H,dtype", [(5, 2, 256, torch.float32), (64, 8, 7168, torch.bfloat16),
                                          (3, 3, 1024, torch.bfloat16)])
-def test_unpermute_reduce(nb, T, k, H, dtype):
+def test_unpermute_reduce(nb, T, k, H, dtype, slot_dtype):
+    """Slot rows in fp32 or a 16-bit type: the 16-bit values widen exactly,
+    so the oracle reduces the stored values themselves."""
     g = torch.Generator().manual_seed(T * k)
     rows = T * k + 7
-    so = torch.randn((rows, H), generator=g) * 3
+    so = (torch.randn((rows, H), generator=g) * 3).to(slot_dtype)
     slot_of = torch.randperm(rows, generator=g)[:T * k].to(torch.int32)
     w = torch.rand((T, k), generator=g)
     y = nb.unpermute_reduce(so.to(DEV), slot_of.to(DEV), w.to(DEV), out_dtype=dtype)
-    want = omoe.unpermute_reduce(so.numpy(), slot_of.numpy(), w.numpy())
+    want = omoe.unpermute_reduce(so.double().numpy(), slot_of.numpy(), w.numpy())
     got = y.float().cpu().numpy()
     if dtype == torch.float32:
         assert_rows_close(got, want, "y")
