@@ -633,6 +633,34 @@ __device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t 
 // (column j = A row 32 j + l).  The slot is free once the stage's loads
 // have landed: the producer refills a stage only after the MMAs that read
 // its previous scales have completed.
+// One stage's scales into this warp's TMEM lanes (the stage's loads have
+// landed), then the warp's arrival on the stage's sf_full barrier.
+__device__ __forceinline__ void write_stage_sf(int stage, Barriers* bars, const uint8_t* smem,
+                                               uint32_t lane_base) {
+  const int lane = threadIdx.x & 31;
+  const uint4* sa = reinterpret_cast<const uint4*>(smem + kOffSfa + stage * kSfaBytes) + lane;
+  const uint4* sb = reinterpret_cast<const uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane;
+  uint32_t a[16], b[32];
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    const uint4 v = sa[kb * 32];                       // atom kb, row l
+    a[4 * kb] = v.x; a[4 * kb + 1] = v.y; a[4 * kb + 2] = v.z; a[4 * kb + 3] = v.w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = sb[h * 128 + kb * 32];           // half h, atom kb, row l
+      b[8 * kb + 4 * h] = u.x; b[8 * kb + 4 * h + 1] = u.y;
+      b[8 * kb + 4 * h + 2] = u.z; b[8 * kb + 4 * h + 3] = u.w;
+    }
+  }
+  const uint32_t col = kTmemSf + stage * kTmemSfStage;
+  tmem_st_32x32b_x32(lane_base + col, b);
+  tmem_st_32x32b_x16(lane_base + col + 32, a);
+  tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars->sf_full[stage]);
+}
+
 __device__ bool run_sf_writer(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t tmem,
                               Pipe& pp, volatile int* abort) {
   const GemmArgs& args = *P.a;
@@ -645,28 +673,7 @@ __device__ bool run_sf_writer(const Phase& P, Barriers* bars, uint8_t* smem, uin
   while (it.next(tile, s0, s1)) {
     for (int ks = s0; ks < s1; ++ks) {
       if (!mbar_wait(&bars->full[pp.stage], pp.phase, args.status, abort)) return false;
-      const int stage = pp.stage;
-      const uint4* sa = reinterpret_cast<const uint4*>(smem + kOffSfa + stage * kSfaBytes) + lane;
-      const uint4* sb = reinterpret_cast<const uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane;
-      uint32_t a[16], b[32];
-#pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        const uint4 v = sa[kb * 32];                       // atom kb, row l
-        a[4 * kb] = v.x; a[4 * kb + 1] = v.y; a[4 * kb + 2] = v.z; a[4 * kb + 3] = v.w;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 u = sb[h * 128 + kb * 32];           // half h, atom kb, row l
-          b[8 * kb + 4 * h] = u.x; b[8 * kb + 4 * h + 1] = u.y;
-          b[8 * kb + 4 * h + 2] = u.z; b[8 * kb + 4 * h + 3] = u.w;
-        }
-      }
-      const uint32_t col = kTmemSf + stage * kTmemSfStage;
-      tmem_st_32x32b_x32(lane_base + col, b);
-      tmem_st_32x32b_x16(lane_base + col + 32, a);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->sf_full[stage]);
+      write_stage_sf(pp.stage, bars, smem, lane_base);
       if (++pp.stage == kStages) {
         pp.stage = 0;
         pp.phase ^= 1u;
