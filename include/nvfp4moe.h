@@ -382,7 +382,12 @@ int moe_nvfp4_forward(const nvmoe_weights* weights, const uint8_t* xq,
  *                   probability of the selected expert
  *   x bf16 [T, H];  w_router bf16 [E, H];  topk_ids int32 [T, k];
  *   topk_w float [T, k]
- * Workspace: moe_router_workspace_size(T, H, E) bytes (no zero-fill needed).
+ * The logits run on the tensor cores (tcgen05.mma kind::f16, fp32
+ * accumulation in TMEM): a CTA takes 128 tokens and one range of H, and the
+ * ranges' partial logits are added in range order (so results do not depend
+ * on timing); small batches split H over several CTAs.
+ * Workspace: moe_router_workspace_size(T, H, E) bytes; its first word is a
+ * status word (nvmoe_read_status), zero before the first use.
  * Limits: H % 128 == 0, 1 <= E <= 256, 1 <= k <= min(E, 32); x and w_router
  * 16-byte aligned.
  */

@@ -519,7 +519,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
 // ------------------------------------------------------------ router ----
 size_t moe_router_workspace_size(int64_t T, int H, int E) {
   if (T < 0 || H < 1 || E < 1 || !elems_fit(T, H)) return 0;
-  return router_workspace_bytes(T, H, E);
+  return kStatusBytes + align_up(router_workspace_bytes(T, H, E));
 }
 
 int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E, int k,
@@ -536,8 +536,18 @@ int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E
     return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(ws)) return NVMOE_ERR_MISALIGNED;
   if (ws_bytes < moe_router_workspace_size(T, H, E)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
-  return status_of(counted(launch_router(x, w_router, T, H, E, k, softmax_mode, topk_ids,
-                                         topk_w, static_cast<float*>(ws), stream),
+  // x and the weight as byte matrices [rows, 2H]: 64 bf16 per 128-byte box
+  // row; the weight box spans E rounded up to 16 rows (the rows past E are
+  // filled with zeros)
+  CUtensorMap map_x, map_w;
+  if (!make_map(&map_x, x, int64_t{2} * H, T, 128) ||
+      !make_map(&map_w, w_router, int64_t{2} * H, E, static_cast<uint32_t>((E + 15) / 16 * 16)))
+    return NVMOE_ERR_CUDA;
+  Carve c{static_cast<uint8_t*>(ws)};
+  int* status = c.take<int>(kStatusBytes);
+  float* partials = c.take<float>(router_workspace_bytes(T, H, E));
+  return status_of(counted(launch_router(map_x, map_w, T, H, E, k, softmax_mode, topk_ids,
+                                         topk_w, partials, status, stream),
                            2));
 }
 

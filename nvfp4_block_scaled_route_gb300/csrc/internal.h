@@ -183,8 +183,11 @@ cudaError_t launch_mma_probe(int variant, int iters, int grid, long long* cycles
 // Router front-end (router.cu): logits partials [splits][T][E] fp32 in the
 // workspace, then top-k and softmax per token.
 size_t router_workspace_bytes(int64_t T, int H, int E);
-cudaError_t launch_router(const void* x, const void* w, int64_t T, int H, int E, int k, int mode,
-                          int32_t* ids, float* weights, float* partials, cudaStream_t stream);
+// map_x: x as bytes [T, 2H], box 128 B x 128 rows; map_w: the router weight
+// as bytes [E, 2H], box 128 B x (E padded to 16) rows; both 128-byte swizzle.
+cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, int64_t T, int H,
+                          int E, int k, int mode, int32_t* ids, float* weights, float* partials,
+                          int* status, cudaStream_t stream);
 
 cudaError_t launch_reduce(const void* slot_out, int slot_dtype, const int32_t* slot_of,
                           const float* topk_w, int64_t T, int k, int64_t H, void* y, int y_dtype,

@@ -1,274 +1,165 @@
 // Router front-end: the step before the routing permutation.  For every
-// token, logits = x W_r^T (bf16 inputs, fp32 products and sums), the k
-// largest logits (ties to the lower expert id; slot j in descending-logit
-// order), and their weights from a softmax (over the k selected logits, or
-// the full softmax's probabilities of the selected experts).
-// The pages keep the router ("gate") weight in BF16 (NVFP4 MegaMoE Debug
-// Log, Checkpoint Layers) and the workloads route top-k with softmax
-// weights; the rest is the plain reading of a top-k softmax router.
+// token, logits = x W_r^T (bf16 inputs, fp32 sums), the k largest logits
+// (ties to the lower expert id; slot j in descending-logit order), and their
+// weights from a softmax (over the k selected logits, or the full softmax's
+// probabilities of the selected experts).  The pages keep the router
+// ("gate") weight in BF16 ("NVFP4 MegaMoE Debug Log", Checkpoint Layers) and
+// the workloads route top-k with softmax weights; the rest is the plain
+// reading of a top-k softmax router.
 //
-// Two launches.  router_logits_kernel: a CTA takes 32 tokens x all experts
-// x one K range and accumulates in K order; small batches split K over many
-// CTAs (the router weight is the bulk of the bytes), each range's partial
-// logits go to the workspace.  router_topk_kernel: one warp per token sums
-// the partials in range order (deterministic), selects and normalises.
+// Two launches.
+//  * router_tc_kernel: the logits on the 5th-generation tensor cores.  A CTA
+//    takes a tile of 128 tokens and one range of K: TMA brings the x tile
+//    (128 x 64 bf16) and the router weight (E padded to a multiple of 16
+//    rows x 64 bf16) stage by stage in the 128-byte-swizzled K-major layout,
+//    one thread issues tcgen05.mma.kind::f16 (M = 128, N = E padded, K = 16)
+//    into an fp32 accumulator in TMEM, and the four warps read it back
+//    (tcgen05.ld) into the workspace as that range's partial logits.  The
+//    logits are HBM-bound (48 flops per byte of x at E = 48), so the grid is
+//    sized to stream from every SM: about two CTAs per SM, small batches
+//    splitting K over several CTAs (the weight is then most of the bytes).
+//  * router_topk_kernel: one warp per token sums the partials in range order
+//    (deterministic), selects the top k and normalises.
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace nvmoe {
 namespace {
 
-constexpr int kRouterThreads = 256;
-constexpr int kTokPerCta = 32;
-constexpr int kChunkK = 128;          // K elements staged per step
-constexpr int kXStride = kChunkK + 2; // padded row (bf16): no bank conflicts across tokens
+constexpr int kSms = 152;                 // grid sizing target (GB300)
+constexpr int kRtRows = 128;              // tokens per tile (MMA M)
+constexpr int kRtK = 64;                  // K elements per stage (128 bytes of bf16)
+constexpr int kRtStages = 4;
+constexpr int kRtMinStages = 4;           // stages per CTA at least (fewer partials)
+constexpr int kRtThreads = 128;
+constexpr int kRtXBytes = kRtRows * 128;  // 16 KB
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+struct RtBars {
+  uint64_t full[kRtStages];
+  uint64_t empty[kRtStages];
+  uint64_t done;
+  uint32_t tmem;
+  int abort;
+};
 
-// partials[split][t][e] = sum over this split's K range, ascending k.
-// NE: experts per thread (compile-time, so the accumulators stay in
-// registers); thread group eg takes experts eg, eg + 8, ...
-template <int NE>
-__global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w, int64_t T, int H,
-    int E, int k_per_split, float* __restrict__ partials) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);                    // [32][kXStride]
-  __nv_bfloat16* ws = xs + kTokPerCta * kXStride;                                 // [E][kChunkK]
-  const int t_local = threadIdx.x & 31;
-  const int eg = threadIdx.x >> 5;                 // expert group 0..7: experts eg, eg+8, ...
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokPerCta;
-  const int k0 = blockIdx.y * k_per_split;
-  const int k1 = min(H, k0 + k_per_split);
-  constexpr int kMaxPerThread = NE;
-  float acc[kMaxPerThread];
-#pragma unroll
-  for (int i = 0; i < kMaxPerThread; ++i) acc[i] = 0.0f;
-  const int n_e = (E - eg + 7) / 8;                // experts of this thread's group
-  for (int kc = k0; kc < k1; kc += kChunkK) {
-    __syncthreads();
-    // stage x[t0..t0+31][kc..kc+127] (pairs of bf16) and W[0..E-1][kc..kc+127]
-    for (int i = threadIdx.x; i < kTokPerCta * (kChunkK / 2); i += kRouterThreads) {
-      const int r = i / (kChunkK / 2), c = (i % (kChunkK / 2)) * 2;
-      uint32_t v = 0;
-      if (t0 + r < T)
-        v = *reinterpret_cast<const uint32_t*>(x + (t0 + r) * H + kc + c);
-      *reinterpret_cast<uint32_t*>(xs + r * kXStride + c) = v;
-    }
-    for (int i = threadIdx.x; i < E * (kChunkK / 8); i += kRouterThreads) {
-      const int r = i / (kChunkK / 8), c = (i % (kChunkK / 8)) * 8;
-      *reinterpret_cast<uint4*>(ws + r * kChunkK + c) =
-          __ldg(reinterpret_cast<const uint4*>(w + static_cast<int64_t>(r) * H + kc + c));
-    }
-    __syncthreads();
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + t_local * kXStride);
-    for (int c = 0; c < kChunkK / 2; ++c) {
-      const uint32_t xv = xr[c];
-      const float xa = bf_lo(xv), xb = bf_hi(xv);
-#pragma unroll
-      for (int i = 0; i < kMaxPerThread; ++i) {
-        if (i < n_e) {
-          const uint32_t wv =
-              reinterpret_cast<const uint32_t*>(ws + (eg + 8 * i) * kChunkK)[c];
-          acc[i] = __fmaf_rn(xa, bf_lo(wv), acc[i]);
-          acc[i] = __fmaf_rn(xb, bf_hi(wv), acc[i]);
-        }
-      }
-    }
-  }
-  const int64_t t = t0 + t_local;
-  if (t < T) {
-    float* out = partials + (static_cast<int64_t>(blockIdx.y) * T + t) * E;
-#pragma unroll
-    for (int i = 0; i < kMaxPerThread; ++i)
-      if (i < n_e) out[eg + 8 * i] = acc[i];
-  }
+__host__ __device__ inline int rt_npad(int E) { return (E + 15) / 16 * 16; }
+__host__ __device__ inline int rt_stage_bytes(int E) { return kRtXBytes + rt_npad(E) * 128; }
+inline size_t rt_smem_bytes(int E) {
+  return static_cast<size_t>(kRtStages) * rt_stage_bytes(E) + 1024 + sizeof(RtBars);
 }
 
-// Small batches (T <= kSmallT): one CTA per expert streams that expert's
-// weight row once; thread i owns the 8-element groups i, i + 128, ... of H
-// and accumulates every token over them; the 128 partial sums of a logit are
-// then added in a fixed tree (warp shuffles, then the four warps in order).
-constexpr int kSmallT = 32;
-constexpr int kSms = 152;               // grid sizing target (GB300)
-constexpr int kMmaMinT = 1024;          // tensor-core logits from this many tokens
-constexpr int kSmallThreads = 128;
+// TMEM columns for the accumulator: a power of two >= max(32, N).
+__device__ __forceinline__ uint32_t rt_tmem_cols(int n) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(n)) c <<= 1;
+  return c;
+}
 
-template <int TT>
-__global__ void __launch_bounds__(kSmallThreads) router_logits_small_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w, int T, int H,
-    int E, float* __restrict__ logits) {
-  __shared__ float red[kSmallThreads / 32][TT];
-  const int e = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float acc[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
-  const uint4* wr = reinterpret_cast<const uint4*>(w + static_cast<int64_t>(e) * H);
-  const int groups = H / 8;
-  // blocks of 8 groups per thread: all loads of a block are issued before
-  // any is used (one memory round trip per block, not per group)
-  for (int g0 = threadIdx.x; g0 < groups; g0 += 8 * kSmallThreads) {
-    uint4 wv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int g = g0 + j * kSmallThreads;
-      wv[j] = g < groups ? __ldg(wr + g) : make_uint4(0u, 0u, 0u, 0u);
+__global__ void __launch_bounds__(kRtThreads) router_tc_kernel(
+    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+    int64_t T, int E, int stages_total, int stages_per_split, float* __restrict__ partials,
+    int* status) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+  const int n_pad = rt_npad(E);
+  const int stage_bytes = rt_stage_bytes(E);
+  RtBars* bars = reinterpret_cast<RtBars*>(smem + kRtStages * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int ks0 = split * stages_per_split;
+  const int ks1 = min(stages_total, ks0 + stages_per_split);
+  const uint32_t ncols = rt_tmem_cols(n_pad);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
     }
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      if (t < T) {
-        const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
-        uint4 xv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int g = g0 + j * kSmallThreads;
-          xv[j] = g < groups ? __ldg(xr + g) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-          const uint32_t x4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            acc[t] = __fmaf_rn(bf_lo(x4[m]), bf_lo(w4[m]), acc[t]);
-            acc[t] = __fmaf_rn(bf_hi(x4[m]), bf_hi(w4[m]), acc[t]);
-          }
-        }
-      }
-    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbarrier_init();
+    prefetch_tensormap(&map_x);
+    prefetch_tensormap(&map_w);
   }
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    float v = acc[t];
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if (lane == 0) red[warp][t] = v;
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem, ncols);
+    tmem_relinquish();
   }
+  tc_fence_before();
   __syncthreads();
-  if (threadIdx.x < T) {
-    const int t = threadIdx.x;
-    float v = 0.0f;
-#pragma unroll
-    for (int q = 0; q < kSmallThreads / 32; ++q) v += red[q][t];
-    logits[static_cast<int64_t>(t) * E + e] = v;
-  }
-}
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
 
-// Larger batches: the logits as a tensor-core contraction.  A CTA takes 128
-// tokens (8 warps x 16 rows) and a column tile of NT x 8 experts
-// (blockIdx.y), and walks H in chunks of 64 that cp.async stages into a
-// four-deep shared-memory ring (three chunks in flight while one is used);
-// each warp issues mma.sync.m16n8k16 (bf16 in, fp32 accumulate) over its 16
-// rows.  The K order is fixed, so the logits do not depend on timing.
-constexpr int kMmaRows = 128;
-constexpr int kMmaK = 64;
-constexpr int kMmaStride = kMmaK + 8;   // bf16 per staged row (+16 B: no bank conflicts)
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, bool valid) {
-  // 16 bytes global -> shared, zero-filled when !valid (src is then not read)
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-constexpr int kMmaStages = 4;
-
-template <int NT>
-__global__ void __launch_bounds__(256) router_logits_mma_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w, int64_t T, int H,
-    int E, float* __restrict__ logits) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  constexpr int kStageElems = (kMmaRows + NT * 8) * kMmaStride;
-  __nv_bfloat16* stage_base = reinterpret_cast<__nv_bfloat16*>(smem);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int grp = lane >> 2, tig = lane & 3;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kMmaRows;
-  const int e0 = blockIdx.y * NT * 8;     // first expert of this CTA's column tile
-  const int chunks = H / kMmaK;
-  // chunk c -> stage c % kMmaStages: 128 token rows then NT*8 expert rows
-  auto load = [&](int c) {
-    __nv_bfloat16* xs = stage_base + (c % kMmaStages) * kStageElems;
-    __nv_bfloat16* ws = xs + kMmaRows * kMmaStride;
-    const int kc = c * kMmaK;
-    for (int i = threadIdx.x; i < kMmaRows * (kMmaK / 8); i += 256) {
-      const int r = i / (kMmaK / 8), col = (i % (kMmaK / 8)) * 8;
-      const bool ok = t0 + r < T;
-      cp_async16(xs + r * kMmaStride + col, x + (ok ? (t0 + r) * H + kc + col : 0), ok);
-    }
-    for (int i = threadIdx.x; i < NT * 8 * (kMmaK / 8); i += 256) {
-      const int r = i / (kMmaK / 8), col = (i % (kMmaK / 8)) * 8;
-      const bool ok = e0 + r < E;
-      cp_async16(ws + r * kMmaStride + col,
-                 w + (ok ? static_cast<int64_t>(e0 + r) * H + kc + col : 0), ok);
-    }
-  };
-  float acc[NT][4];
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[n][i] = 0.0f;
-#pragma unroll
-  for (int c = 0; c < kMmaStages - 1; ++c) {
-    if (c < chunks) load(c);
-    cp_async_commit();
-  }
-  for (int c = 0; c < chunks; ++c) {
-    cp_async_wait<kMmaStages - 2>();          // chunk c has landed (this thread's part)
-    __syncthreads();                           // ... and everyone's; stage of c-1 is free
-    if (c + kMmaStages - 1 < chunks) load(c + kMmaStages - 1);
-    cp_async_commit();
-    const __nv_bfloat16* xs = stage_base + (c % kMmaStages) * kStageElems;
-    const __nv_bfloat16* ws = xs + kMmaRows * kMmaStride;
-    const __nv_bfloat16* xw = xs + (warp * 16) * kMmaStride;
-#pragma unroll
-    for (int k16 = 0; k16 < kMmaK; k16 += 16) {
-      uint32_t a[4];
-      a[0] = *reinterpret_cast<const uint32_t*>(xw + grp * kMmaStride + k16 + 2 * tig);
-      a[1] = *reinterpret_cast<const uint32_t*>(xw + (grp + 8) * kMmaStride + k16 + 2 * tig);
-      a[2] = *reinterpret_cast<const uint32_t*>(xw + grp * kMmaStride + k16 + 8 + 2 * tig);
-      a[3] = *reinterpret_cast<const uint32_t*>(xw + (grp + 8) * kMmaStride + k16 + 8 + 2 * tig);
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const __nv_bfloat16* wr = ws + (n * 8 + grp) * kMmaStride + k16 + 2 * tig;
-        uint32_t b[2];
-        b[0] = *reinterpret_cast<const uint32_t*>(wr);
-        b[1] = *reinterpret_cast<const uint32_t*>(wr + 8);
-        mma_bf16_16816(acc[n], a, b);
+  if (warp == 0 && lane == 0) {
+    // producer: x tile and the weight rows of each stage of this K range
+    const uint64_t pol_x = policy_evict_first();
+    const uint64_t pol_w = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int ks = ks0; ks < ks1; ++ks) {
+      if (!mbar_wait(&bars->empty[stage], phase ^ 1u, status, abort)) break;
+      uint8_t* xs = smem + stage * stage_bytes;
+      mbar_arrive_expect_tx(&bars->full[stage], static_cast<uint32_t>(stage_bytes));
+      tma_load_2d(xs, &map_x, ks * 128, tile * kRtRows, &bars->full[stage], pol_x);
+      tma_load_2d(xs + kRtXBytes, &map_w, ks * 128, 0, &bars->full[stage], pol_w);
+      if (++stage == kRtStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: four K = 16 steps per stage, in K order
+    const uint32_t idesc = idesc_bf16_f32(kRtRows, n_pad);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int ks = ks0; ks < ks1 && ok; ++ks) {
+      if (!mbar_wait(&bars->full[stage], phase, status, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t xa = smem_u32(smem + stage * stage_bytes);
+      const uint32_t wa = xa + kRtXBytes;
+#pragma unroll
+      for (int kk = 0; kk < kRtK / 16; ++kk)
+        mma_f16(tmem, smem_desc(xa + kk * 32, 16, 1024, 2), smem_desc(wa + kk * 32, 16, 1024, 2),
+                idesc, (ks != ks0 || kk != 0) ? 1u : 0u);
+      tc_commit(&bars->empty[stage]);
+      if (++stage == kRtStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    tc_commit(&bars->done);
   }
-  cp_async_wait<0>();
-  // D fragment: rows grp / grp + 8 of the warp's 16, columns 2*tig, 2*tig + 1
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const int e = e0 + n * 8 + 2 * tig;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t t = t0 + warp * 16 + grp + 8 * h;
+  // epilogue: every warp reads its 32 TMEM lanes (token rows)
+  __syncwarp();
+  const bool ok = mbar_wait(&bars->done, 0, status, abort);
+  tc_fence_after();
+  if (ok) {
+    const int64_t t = static_cast<int64_t>(tile) * kRtRows + warp * 32 + lane;
+    float* out = partials + (static_cast<int64_t>(split) * T + t) * E;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c = 0; c < n_pad; c += 16) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(trow + c, r);
+      tmem_ld_wait();
       if (t < T) {
-        if (e < E) logits[t * E + e] = acc[n][2 * h];
-        if (e + 1 < E) logits[t * E + e + 1] = acc[n][2 * h + 1];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c + j < E) out[c + j] = __uint_as_float(r[j]);
       }
     }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
   }
 }
 
@@ -359,105 +250,48 @@ __global__ void router_topk_kernel(const float* __restrict__ partials, int split
   }
 }
 
-int splits_for(int64_t T, int H) {
-  if (T <= kSmallT || T >= kMmaMinT) return 1;
-  const int64_t tiles = (T + kTokPerCta - 1) / kTokPerCta;
+// K ranges: about two CTAs per SM over (token tiles x ranges), whole stages
+// per range, at least kRtMinStages of them (the top-k adds every range's
+// partials).
+int router_splits(int64_t T, int H) {
+  const int64_t tiles = (T + kRtRows - 1) / kRtRows;
+  const int stages = H / kRtK;
   int64_t s = (2 * kSms) / (tiles > 0 ? tiles : 1);
-  const int max_s = H / kChunkK;
+  const int64_t max_s = stages / kRtMinStages > 0 ? stages / kRtMinStages : 1;
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
-  return static_cast<int>(s);
+  const int per = static_cast<int>((stages + s - 1) / s);
+  return (stages + per - 1) / per;
 }
+
+PerDeviceOnce g_router_attr;
 
 }  // namespace
 
 size_t router_workspace_bytes(int64_t T, int H, int E) {
-  return static_cast<size_t>(splits_for(T, H)) * static_cast<size_t>(T) * E * sizeof(float);
+  return static_cast<size_t>(router_splits(T, H)) * static_cast<size_t>(T) * E * sizeof(float);
 }
 
-cudaError_t launch_router(const void* x, const void* w, int64_t T, int H, int E, int k, int mode,
-                          int32_t* ids, float* weights, float* partials, cudaStream_t stream) {
+cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, int64_t T, int H,
+                          int E, int k, int mode, int32_t* ids, float* weights, float* partials,
+                          int* status, cudaStream_t stream) {
+  const int stages = H / kRtK;
+  const int splits = router_splits(T, H);
+  const int per = (stages + splits - 1) / splits;
+  const size_t smem = rt_smem_bytes(E);
+  // the attribute is the largest any E takes (set once per device)
+  cudaError_t e = set_smem_attr_once(g_router_attr,
+                                     reinterpret_cast<const void*>(router_tc_kernel),
+                                     static_cast<int>(rt_smem_bytes(kMaxExperts)));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>((T + kRtRows - 1) / kRtRows), static_cast<unsigned>(splits));
+  router_tc_kernel<<<grid, kRtThreads, smem, stream>>>(map_x, map_w, T, E, stages, per, partials,
+                                                       status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int warps = 8;
-  if (T <= kSmallT) {
-    const auto* xb = static_cast<const __nv_bfloat16*>(x);
-    const auto* wb = static_cast<const __nv_bfloat16*>(w);
-    const int t = static_cast<int>(T);
-    if (T <= 4)
-      router_logits_small_kernel<4><<<E, kSmallThreads, 0, stream>>>(xb, wb, t, H, E, partials);
-    else if (T <= 8)
-      router_logits_small_kernel<8><<<E, kSmallThreads, 0, stream>>>(xb, wb, t, H, E, partials);
-    else if (T <= 16)
-      router_logits_small_kernel<16><<<E, kSmallThreads, 0, stream>>>(xb, wb, t, H, E, partials);
-    else
-      router_logits_small_kernel<32><<<E, kSmallThreads, 0, stream>>>(xb, wb, t, H, E, partials);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    router_topk_kernel<<<static_cast<unsigned>((T + warps - 1) / warps), warps * 32, 0, stream>>>(
-        partials, 1, T, E, k, mode, ids, weights);
-    return cudaGetLastError();
-  }
-  if (T >= kMmaMinT && H % kMmaK == 0) {
-    const auto* xb = static_cast<const __nv_bfloat16*>(x);
-    const auto* wb = static_cast<const __nv_bfloat16*>(w);
-    // column tile: all experts in one CTA, halved (down to 64 experts) while
-    // the grid would leave SMs idle; x tiles are then re-read from L2
-    const int nt_all = (E + 7) / 8;
-    int nt = nt_all <= 2 ? 2 : nt_all <= 4 ? 4 : nt_all <= 6 ? 6 : nt_all <= 8 ? 8
-           : nt_all <= 16 ? 16 : 32;
-    const int64_t row_tiles = (T + kMmaRows - 1) / kMmaRows;
-    while (nt > 8 && row_tiles * ((nt_all + nt - 1) / nt) < kSms) nt /= 2;
-    const size_t smem =
-        static_cast<size_t>(kMmaStages) * (kMmaRows + nt * 8) * kMmaStride * 2;
-    const dim3 grid(static_cast<unsigned>(row_tiles),
-                    static_cast<unsigned>((nt_all + nt - 1) / nt));
-    auto run = [&](auto kernel) -> cudaError_t {
-      if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-      }
-      kernel<<<grid, 256, smem, stream>>>(xb, wb, T, H, E, partials);
-      return cudaGetLastError();
-    };
-    cudaError_t err = nt == 2 ? run(router_logits_mma_kernel<2>)
-                    : nt == 4 ? run(router_logits_mma_kernel<4>)
-                    : nt == 6 ? run(router_logits_mma_kernel<6>)
-                    : nt == 8 ? run(router_logits_mma_kernel<8>)
-                    : nt == 16 ? run(router_logits_mma_kernel<16>)
-                               : run(router_logits_mma_kernel<32>);
-    if (err != cudaSuccess) return err;
-    router_topk_kernel<<<static_cast<unsigned>((T + warps - 1) / warps), warps * 32, 0, stream>>>(
-        partials, 1, T, E, k, mode, ids, weights);
-    return cudaGetLastError();
-  }
-  const int splits = splits_for(T, H);
-  // K range per split: whole chunks
-  const int chunks = H / kChunkK;
-  const int k_per_split = ((chunks + splits - 1) / splits) * kChunkK;
-  const int used = (H + k_per_split - 1) / k_per_split;
-  const size_t smem = (kTokPerCta * kXStride + static_cast<size_t>(E) * kChunkK) * 2;
-  dim3 grid(static_cast<unsigned>((T + kTokPerCta - 1) / kTokPerCta), used);
-  auto run = [&](auto kernel) -> cudaError_t {
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
-    kernel<<<grid, kRouterThreads, smem, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), T, H, E,
-        k_per_split, partials);
-    return cudaGetLastError();
-  };
-  const int per = (E + 7) / 8;
-  cudaError_t err = per <= 2 ? run(router_logits_kernel<2>)
-                  : per <= 4 ? run(router_logits_kernel<4>)
-                  : per <= 6 ? run(router_logits_kernel<6>)
-                  : per <= 8 ? run(router_logits_kernel<8>)
-                  : per <= 16 ? run(router_logits_kernel<16>)
-                              : run(router_logits_kernel<32>);
-  if (err != cudaSuccess) return err;
   router_topk_kernel<<<static_cast<unsigned>((T + warps - 1) / warps), warps * 32, 0, stream>>>(
-      partials, used, T, E, k, mode, ids, weights);
+      partials, splits, T, E, k, mode, ids, weights);
   return cudaGetLastError();
 }
 
