@@ -81,6 +81,12 @@ typedef enum { NVMOE_BF16 = 0, NVMOE_F32 = 1, NVMOE_F16 = 2 } nvmoe_dtype;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvmoe_status_str(int status);
 
+/* Name of the CUDA error (e.g. "cudaErrorInvalidValue") behind the last
+   NVMOE_ERR_CUDA returned on the calling host thread, or "" if there was
+   none.  Static string, never NULL; the record is per thread and is
+   overwritten by the next failing call.  Host only, no device work. */
+const char* nvmoe_last_cuda_error(void);
+
 /* Library ABI version (major * 100 + minor): 200 (nvmoe_taps gained the
  * ready-flag members). */
 int nvmoe_version(void);

@@ -18,6 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libnvfp4moe.so")
 
 BF16, F32, F16 = 0, 1, 2
+NVMOE_ERR_CUDA = 5
 TILE_ROWS = 128
 
 _lib = None
@@ -27,6 +28,8 @@ class NvmoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
         msg = lib().nvmoe_status_str(status).decode() if _lib is not None else str(status)
+        if status == NVMOE_ERR_CUDA and _lib is not None:
+            msg += f" [{lib().nvmoe_last_cuda_error().decode()}]"
         super().__init__(f"{fn} failed: {msg} (status {status})")
 
 
@@ -52,6 +55,7 @@ PATH_AUTO, PATH_SEPARATE, PATH_FUSED, PATH_LAYER = 0, 1, 2, 3
 _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 SIGNATURES = {
     "nvmoe_status_str": (ctypes.c_char_p, [_I]),
+    "nvmoe_last_cuda_error": (ctypes.c_char_p, []),
     "nvmoe_version": (_I, []),
     "nvmoe_kernel_launch_count": (ctypes.c_uint64, []),
     "nvmoe_read_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),

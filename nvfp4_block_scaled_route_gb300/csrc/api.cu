@@ -76,7 +76,20 @@ int sm_count() {
   return n;
 }
 
-int status_of(cudaError_t e) { return e == cudaSuccess ? NVMOE_OK : NVMOE_ERR_CUDA; }
+// The CUDA error behind the last NVMOE_ERR_CUDA of this host thread.
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+cudaError_t note(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda = e;
+  return e;
+}
+
+int fail(cudaError_t e) {
+  note(e);
+  return NVMOE_ERR_CUDA;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? NVMOE_OK : fail(e); }
 
 // Kernels of this library enqueued so far (CUDA-graph replays are not
 // launches and are not counted).
@@ -84,7 +97,7 @@ std::atomic<uint64_t> g_launches{0};
 
 cudaError_t counted(cudaError_t e, int kernels) {
   if (e == cudaSuccess) g_launches += kernels;
-  return e;
+  return note(e);
 }
 
 }  // namespace
@@ -124,6 +137,10 @@ int64_t rows_bound(int64_t T, int k, int E) {
 
 extern "C" {
 
+const char* nvmoe_last_cuda_error(void) {
+  return g_last_cuda == cudaSuccess ? "" : cudaGetErrorName(g_last_cuda);
+}
+
 const char* nvmoe_status_str(int s) {
   switch (s) {
     case NVMOE_OK: return "ok";
@@ -148,7 +165,7 @@ int nvmoe_read_status(const void* ws, cudaStream_t stream, int* out) {
   int v = 0;
   cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (e != cudaSuccess) return fail(e);
   *out = v;
   return NVMOE_OK;
 }
@@ -252,7 +269,7 @@ int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
                                                 sf_rowmajor, sf_mma, gs_out, stream), 1));
   const int parts = quant_amax_blocks(n);
   cudaError_t e = counted(launch_quant_amax(x, x_dtype, n, partial, parts, stream), 1);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (e != cudaSuccess) return fail(e);
   return status_of(counted(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr,
                                              partial, parts, q, sf_rowmajor, sf_mma, gs_out,
                                              stream), 1));
@@ -279,7 +296,7 @@ int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q, uint
   c.take<int>(kStatusBytes);
   float* partial = c.take<float>(static_cast<size_t>(E) * 64 * sizeof(float));
   cudaError_t e = counted(launch_weight_amax(w, E, static_cast<int64_t>(K) * N, partial, 64, stream), 1);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (e != cudaSuccess) return fail(e);
   return status_of(counted(launch_weight_quant(w, E, K, N, partial, 64, q, sf, gs, stream), 1));
 }
 
@@ -392,7 +409,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   }
   const int64_t rows = rows_bound(T, k, E);
   int nsm = sm_count();
-  if (nsm <= 0) return NVMOE_ERR_CUDA;
+  if (nsm <= 0) return fail(cudaErrorNoDevice);
   if (nsm > kMaxGrid) nsm = kMaxGrid;
 
   AMaps map_x, map_h;
@@ -404,7 +421,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
       !make_map(&map_h.full, b.hq, I / 2, rows) ||
       !make_map(&map_h.small, b.hq, I / 2, rows, kSmallABoxRows) ||
       !make_tiled_map(&map_w2, w->w2, int64_t(E) * H / kTileRows * kt2))
-    return NVMOE_ERR_CUDA;
+    return fail(cudaErrorInvalidValue);  // tensor-map encoding refused
 
   GemmArgs a1{};
   a1.mode = 1;
@@ -465,6 +482,9 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   const int64_t S = T * k;
   const int64_t mt_bound = S / kTileRows + (S < E ? S : E);
   const int64_t tiles1 = mt_bound * a1.n_tiles, tiles2 = mt_bound * a2.n_tiles;
+  // and the tiles that exist whatever the routing: every segment of c rows
+  // takes ceil(c / 128) m-tiles, at least ceil(S / 128) over all experts
+  const int64_t mt_min = (S + kTileRows - 1) / kTileRows;
   auto grid_for = [&](int64_t tiles) {
     int64_t g = tiles < nsm ? tiles : nsm;
     return static_cast<int>(g < 1 ? 1 : g);
@@ -473,46 +493,46 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   const bool fused = path == NVMOE_PATH_FUSED ||
                      (path == NVMOE_PATH_AUTO && tiles1 < 4 * int64_t(nsm) && tiles2 < 4 * int64_t(nsm));
   const bool timed = ev[0] && ev[1] && ev[2] && ev[3];
-  if (timed && cudaEventRecord(ev[0], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && note(cudaEventRecord(ev[0], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
   if (layer != nullptr) {
     layer->hq = b.hq;
     layer->hsf = b.hsf;
     layer->gs_h = b.gs_h;
     const int g = grid_for(tiles1 > tiles2 ? tiles1 : tiles2);
     cudaError_t e = counted(launch_layer(a1, a2, map_x, map_w1, map_h, map_w2, *layer, g, stream), 1);
-    if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+    if (e != cudaSuccess) return fail(e);
     if (timed)
       for (int i = 1; i < 4; ++i)
-        if (cudaEventRecord(ev[i], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+        if (note(cudaEventRecord(ev[i], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
     return NVMOE_OK;
   }
   if (fused) {
     const int g = grid_for(tiles1 > tiles2 ? tiles1 : tiles2);
     cudaError_t e = counted(launch_fused_ffn(a1, a2, map_x, map_w1, map_h, map_w2, b.grid_bar,
                                              row_token, b.hq, b.hsf, b.gs_h, g, stream), 1);
-    if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+    if (e != cudaSuccess) return fail(e);
     if (timed) {
       // one kernel: L1, requantisation and L2 are not separable
       for (int i = 1; i < 4; ++i)
-        if (cudaEventRecord(ev[i], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+        if (note(cudaEventRecord(ev[i], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
     }
     return NVMOE_OK;
   }
   const int g1 = grid_for(tiles1);
-  cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, stream), 1);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
-  if (timed && cudaEventRecord(ev[1], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, mt_min * a1.n_tiles, stream), 1);
+  if (e != cudaSuccess) return fail(e);
+  if (timed && note(cudaEventRecord(ev[1], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
   if (w->gs_mid == nullptr) {
     // requantise h over the valid rows (global amax from the L1 partials);
     // with a static intermediate scale the L1 epilogue has done it
     e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1,
                                   b.hq, nullptr, b.hsf, b.gs_h, stream), 1);
-    if (e != cudaSuccess) return NVMOE_ERR_CUDA;
+    if (e != cudaSuccess) return fail(e);
   }
-  if (timed && cudaEventRecord(ev[2], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
-  e = counted(launch_gemm(a2, map_h, map_w2, grid_for(tiles2), stream), 1);
-  if (e != cudaSuccess) return NVMOE_ERR_CUDA;
-  if (timed && cudaEventRecord(ev[3], stream) != cudaSuccess) return NVMOE_ERR_CUDA;
+  if (timed && note(cudaEventRecord(ev[2], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
+  e = counted(launch_gemm(a2, map_h, map_w2, grid_for(tiles2), mt_min * a2.n_tiles, stream), 1);
+  if (e != cudaSuccess) return fail(e);
+  if (timed && note(cudaEventRecord(ev[3], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
   return NVMOE_OK;
 }
 
@@ -542,7 +562,7 @@ int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E
   CUtensorMap map_x, map_w;
   if (!make_map(&map_x, x, int64_t{2} * H, T, 128) ||
       !make_map(&map_w, w_router, int64_t{2} * H, E, static_cast<uint32_t>((E + 15) / 16 * 16)))
-    return NVMOE_ERR_CUDA;
+    return fail(cudaErrorInvalidValue);  // tensor-map encoding refused
   Carve c{static_cast<uint8_t*>(ws)};
   int* status = c.take<int>(kStatusBytes);
   float* partials = c.take<float>(router_workspace_bytes(T, H, E));
@@ -643,7 +663,7 @@ int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
   const int64_t rows = rows_bound(T, k, E);
 
   int nsm = sm_count();
-  if (nsm <= 0) return NVMOE_ERR_CUDA;
+  if (nsm <= 0) return fail(cudaErrorNoDevice);
   const int64_t mt_bound = S / kTileRows + (S < E ? S : E);
   const bool small = x_dtype == NVMOE_BF16 && S <= kLayerMaxSlots &&
                      T * H <= kQuantSmallElems && mt_bound * (I / 128) < 4 * int64_t(nsm) &&

@@ -74,8 +74,10 @@ constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemBytes = kSmemUsed + 1024;            // alignment slack
 constexpr int kThreads = 192;                           // cooperative kernels
-constexpr int kThreadsSt = 320;                         // grouped_gemm_kernel
+constexpr int kThreadsSt = 320;                         // grouped_gemm_kernel<false>
+constexpr int kThreadsHalf = 448;                       // grouped_gemm_kernel<true>
 constexpr int kSfWarp0 = 6;                             // first scale-writer warp
+constexpr int kEpi2Warp0 = 10;                          // second epilogue set
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kTmemSfStage = 64;
@@ -133,11 +135,11 @@ struct WorkIter {
   int64_t cur, end;   // stream-K: linear stage units
   int t;              // round-robin: next tile
 
-  __device__ void init(int total_tiles, int k_stages, int grid, int cta) {
+  __device__ void init(int total_tiles, int k_stages, int grid, int cta, bool whole = false) {
     total = total_tiles;
     ks = k_stages;
     G = grid;
-    stream_k = total_tiles < kStreamKFactor * grid;
+    stream_k = !whole && total_tiles < kStreamKFactor * grid;
     const int64_t W = static_cast<int64_t>(total_tiles) * k_stages;
     cur = end = 0;
     t = cta;
@@ -188,6 +190,7 @@ struct Phase {
   const CUtensorMap* map_b;
   const int* prefix;
   int total_tiles, k_blocks, k_stages, k_atoms;
+  bool whole_tiles;     // round-robin whole tiles whatever their number
 };
 
 __device__ __forceinline__ Phase make_phase(const GemmArgs& a, const AMaps* ma,
@@ -201,6 +204,7 @@ __device__ __forceinline__ Phase make_phase(const GemmArgs& a, const AMaps* ma,
   p.k_blocks = a.K / 64;
   p.k_stages = (a.K + kStageK - 1) / kStageK;
   p.k_atoms = p.k_stages * 4;
+  p.whole_tiles = false;
   return p;
 }
 
@@ -461,7 +465,7 @@ __device__ bool run_producer(const Phase& P, int E, const Tables& tb, Barriers* 
                              uint8_t* smem, Pipe& pp, volatile int* abort, const Gate* gate) {
   const GemmArgs& args = *P.a;
   WorkIter it;
-  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
   const uint64_t pol_a = policy_evict_last();
   const uint64_t pol_b = policy_evict_first();
   // the caller's activation-ready flag: waited for before anything is
@@ -574,7 +578,7 @@ __device__ bool run_mma(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t 
                         volatile int* abort) {
   const GemmArgs& args = *P.a;
   WorkIter it;
-  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
   const uint32_t idesc = idesc_mxf4nvf4(kBM, kBN);
   int tile, s0, s1;
   while (it.next(tile, s0, s1)) {
@@ -668,7 +672,7 @@ __device__ bool run_sf_writer(const Phase& P, Barriers* bars, uint8_t* smem, uin
   const uint32_t q = (threadIdx.x >> 5) & 3;
   const uint32_t lane_base = tmem + ((q * 32u) << 16);
   WorkIter it;
-  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
   int tile, s0, s1;
   while (it.next(tile, s0, s1)) {
     for (int ks = s0; ks < s1; ++ks) {
@@ -812,7 +816,7 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
   const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
   const bool lead = warp == 2 && lane == 0;
   WorkIter it;
-  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x);
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
   int tile, s0, s1;
   bool have = it.next(tile, s0, s1);
   // the weight scales of the next tile are loaded one tile ahead; the up
@@ -959,6 +963,84 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
   return true;
 }
 
+// grouped_gemm_kernel<true>, where every CTA takes whole tiles: two epilogue sets, warps 2..5 (set 0) and 10..13 (set 1), each one warp
+// per TMEM lane quarter, take half of every tile's output columns (L1: h
+// columns [64 set, 64 set + 64), from gate columns 64 set + c and up
+// columns 128 + 64 set + c; L2: columns [128 set, 128 set + 128)), so a
+// tile's epilogue -- TMEM loads, SiLU*up or alpha, stores -- takes half as
+// long while the tensor pipe waits for the accumulator.  The arithmetic is
+// epi_l1's and epi_l2's.  acc_empty counts the 8 warps.
+__device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Tables& tb,
+                                  Barriers* bars, uint32_t tmem, volatile int* abort,
+                                  float& amax) {
+  const GemmArgs& args = *P.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int set = warp >= kEpi2Warp0 ? 1 : 0;
+  const int row_in_tile = q * 32 + lane;
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const float* gs_b_up = args.gs_b_up != nullptr ? args.gs_b_up : args.gs_b;
+  const bool mid_alpha = args.mode == 2 && args.gs_mid != nullptr;
+  WorkIter it;
+  it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
+  uint32_t acc_phase = 0;
+  int tile, s0, s1;
+  while (it.next(tile, s0, s1)) {
+    const TileInfo ti = decode_tile(tile, P.prefix, tb.mtiles, E);
+    const float gs_m = mid_alpha ? __ldg(args.gs_mid + ti.e) : gs_a;
+    const float alpha = __fmul_rn(gs_m, __ldg(args.gs_b + ti.e));
+    const float alpha_u = __fmul_rn(gs_m, __ldg(gs_b_up + ti.e));
+    if (!mbar_wait(&bars->acc_full, acc_phase, args.status, abort)) return false;
+    tc_fence_after();
+    const bool valid = ti.mt * kBM + row_in_tile < tb.cnt[ti.e];
+    const int64_t row = tb.off[ti.e] + ti.mt * kBM + row_in_tile;
+    const int nv_w = min(32, max(0, tb.cnt[ti.e] - ti.mt * kBM - q * 32));
+    if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
+      // few rows: each row's columns spread over the lanes, as in epi_l1_1
+      const int64_t qrow0 = tb.off[ti.e] + ti.mt * kBM + q * 32;
+      for (int c = 0; c < 2; ++c) {
+        float g[32], u[32];
+        tmem_ld_f32(t_row + set * 64 + c * 32, g);
+        tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
+        for (int r = 0; r < nv_w; ++r)
+          epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u, qrow0 + r,
+                   ti.nt * 128 + set * 64 + c * 32 + lane, args, amax);
+      }
+    } else if (args.mode == 1 && nv_w > 0) {
+      for (int c = 0; c < 2; ++c) {
+        float g[32], u[32];
+        tmem_ld_f32(t_row + set * 64 + c * 32, g);
+        tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
+        if (valid) epi_l1(g, u, alpha, alpha_u, row, ti.nt * 128 + set * 64 + c * 32, args, amax);
+      }
+    } else if (args.mode != 1 && nv_w > 0) {
+      for (int c = 0; c < 4; ++c) {
+        float a[32];
+        tmem_ld_f32(t_row + set * 128 + c * 32, a);
+        if (valid) epi_l2(a, alpha, row, ti.nt * kBN + set * 128 + c * 32, args);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->acc_empty);
+    acc_phase ^= 1u;
+  }
+  return true;
+}
+
+// The two epilogue sets' per-CTA amax of h -> amax_partial[blockIdx.x].
+__device__ void publish_amax_half(float amax, float* s_amax, float* out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  amax = warp_max(amax);
+  if (lane == 0) s_amax[(warp >= kEpi2Warp0 ? 4 : 0) + (warp & 3)] = amax;
+  asm volatile("bar.sync 2, 256;" ::: "memory");
+  if (warp == 2 && lane == 0) {
+    float m = 0.0f;
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, s_amax[i]);
+    out[blockIdx.x] = m;
+  }
+}
+
 // Per-CTA amax of the L1 epilogue -> amax_partial[blockIdx.x] (epilogue warps).
 __device__ void publish_amax(float amax, float* s_amax, float* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -996,7 +1078,8 @@ __device__ void load_tables(Tables& tb, const GemmArgs& a1, int n_tiles2) {
 }
 
 __device__ uint32_t setup_cta(Barriers* bars, const CUtensorMap* m0, const CUtensorMap* m1,
-                              const CUtensorMap* m2, const CUtensorMap* m3) {
+                              const CUtensorMap* m2, const CUtensorMap* m3,
+                              uint32_t acc_empty_arrivals = 4) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -1005,7 +1088,7 @@ __device__ uint32_t setup_cta(Barriers* bars, const CUtensorMap* m0, const CUten
       mbar_init(&bars->sf_full[s], 4);
     }
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 4);
+    mbar_init(&bars->acc_empty, acc_empty_arrivals);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbarrier_init();
@@ -1046,21 +1129,23 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 }
 
 // ------------------------------------------------------------- kernels --
-__global__ void __launch_bounds__(kThreadsSt, 1) grouped_gemm_kernel(
+template <bool kHalf>
+__global__ void __launch_bounds__(kHalf ? kThreadsHalf : kThreadsSt, 1) grouped_gemm_kernel(
     const __grid_constant__ AMaps map_a, const __grid_constant__ CUtensorMap map_b,
     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
   __shared__ Tables tb;
-  __shared__ float s_amax[4];
+  __shared__ float s_amax[8];
   __shared__ int s_last, s_ok;
 
   load_tables(tb, args, args.n_tiles);
-  const uint32_t tmem = setup_cta(bars, &map_a.full, &map_b, &map_a.small, nullptr);
+  const uint32_t tmem = setup_cta(bars, &map_a.full, &map_b, &map_a.small, nullptr, kHalf ? 8u : 4u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars->abort;
-  const Phase P = make_phase(args, &map_a, &map_b, tb.prefix1, args.E);
+  Phase P = make_phase(args, &map_a, &map_b, tb.prefix1, args.E);
+  P.whole_tiles = kHalf;
   Pipe pp;
   if (warp == 0) {
     if (lane == 0) {
@@ -1072,8 +1157,12 @@ __global__ void __launch_bounds__(kThreadsSt, 1) grouped_gemm_kernel(
       run_mma<true>(P, bars, smem, tmem, pp, abort);
       mma_drain(bars, args.status);
     }
-  } else if (warp >= kSfWarp0) {
+  } else if (warp >= kSfWarp0 && warp < kEpi2Warp0) {
     run_sf_writer(P, bars, smem, tmem, pp, abort);
+  } else if constexpr (kHalf) {
+    float amax = 0.0f;
+    run_epilogue_half(P, __ldcg(args.gs_a), args.E, tb, bars, tmem, abort, amax);
+    if (args.mode == 1) publish_amax_half(amax, s_amax, args.amax_partial);
   } else {
     float amax = 0.0f;
     run_epilogue(P, __ldcg(args.gs_a), args.E, tb, bars, tmem, pp, abort, amax, &s_ok, &s_last);
@@ -1610,7 +1699,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   }
 }
 
-PerDeviceOnce g_gemm_attr, g_fused_attr, g_layer_attr;
+PerDeviceOnce g_gemm_attr, g_gemm_half_attr, g_fused_attr, g_layer_attr;
 
 }  // namespace
 
@@ -1642,13 +1731,22 @@ cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& ma
 int gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
-                        int grid, cudaStream_t stream) {
-  {
-    const cudaError_t err =
-        set_smem_attr_once(g_gemm_attr, reinterpret_cast<const void*>(grouped_gemm_kernel), kSmemBytes);
+                        int grid, int64_t min_tiles, cudaStream_t stream) {
+  // At least kStreamKFactor tiles per CTA whatever the routing, and no
+  // requantisation inside the epilogue: whole tiles and two epilogue sets.
+  const bool half = min_tiles >= int64_t{kStreamKFactor} * grid &&
+                    !(args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue);
+  if (half) {
+    const cudaError_t err = set_smem_attr_once(
+        g_gemm_half_attr, reinterpret_cast<const void*>(grouped_gemm_kernel<true>), kSmemBytes);
     if (err != cudaSuccess) return err;
+    grouped_gemm_kernel<true><<<grid, kThreadsHalf, kSmemBytes, stream>>>(map_a, map_b, args);
+    return cudaGetLastError();
   }
-  grouped_gemm_kernel<<<grid, kThreadsSt, kSmemBytes, stream>>>(map_a, map_b, args);
+  const cudaError_t err = set_smem_attr_once(
+      g_gemm_attr, reinterpret_cast<const void*>(grouped_gemm_kernel<false>), kSmemBytes);
+  if (err != cudaSuccess) return err;
+  grouped_gemm_kernel<false><<<grid, kThreadsSt, kSmemBytes, stream>>>(map_a, map_b, args);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,7 @@ def test_host_side_helpers(lib):
     assert lib.nvmoe_version() >= 100
     assert lib.nvmoe_status_str(0) == b"ok"
     assert lib.nvmoe_status_str(4) == b"workspace too small"
+    assert lib.nvmoe_last_cuda_error() == b""
     # rows bound: S + min(E, S) * 127 rounded up to 128
     assert lib.moe_route_rows_bound(1, 8, 48) == 1024
     assert lib.moe_route_rows_bound(0, 8, 48) == 0
