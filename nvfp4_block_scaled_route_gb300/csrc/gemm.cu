@@ -963,13 +963,54 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
   return true;
 }
 
-// grouped_gemm_kernel<true>, where every CTA takes whole tiles: two epilogue sets, warps 2..5 (set 0) and 10..13 (set 1), each one warp
-// per TMEM lane quarter, take half of every tile's output columns (L1: h
-// columns [64 set, 64 set + 64), from gate columns 64 set + c and up
-// columns 128 + 64 set + c; L2: columns [128 set, 128 set + 128)), so a
-// tile's epilogue -- TMEM loads, SiLU*up or alpha, stores -- takes half as
-// long while the tensor pipe waits for the accumulator.  The arithmetic is
-// epi_l1's and epi_l2's.  acc_empty counts the 8 warps.
+// Lane groups of four (lanes 4g..4g+3) exchange 8-word blocks so that rows
+// leave in 128-byte pieces: before, lane 4g+p holds row 4g+p as blocks
+// v[0..3]; after, lane 4g+p holds block p of rows 4g+0..3 in v[0..3].  Two
+// xor-shuffle rounds (lane bit 1, then bit 0), each sending the half of the
+// blocks the partner keeps; one shuffle per word.
+__device__ __forceinline__ void quad_transpose(uint32_t (&v)[4][8]) {
+  const int lane = threadIdx.x & 31;
+  const bool hi = (lane & 2) != 0, lo = (lane & 1) != 0;
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint32_t r = __shfl_xor_sync(0xffffffffu, hi ? v[b][w] : v[b + 2][w], 2);
+      if (hi) v[b][w] = r;
+      else v[b + 2][w] = r;
+    }
+#pragma unroll
+  for (int rb = 0; rb < 2; ++rb)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint32_t r = __shfl_xor_sync(0xffffffffu, lo ? v[2 * rb][w] : v[2 * rb + 1][w], 1);
+      if (lo) v[2 * rb][w] = r;
+      else v[2 * rb + 1][w] = r;
+    }
+}
+
+// After quad_transpose: lane 4g+p stores its block p of rows 4g+r (r = 0..3)
+// at base + (row0 + 4g + r) * stride + 32 p bytes, rows past n_valid skipped.
+// One instruction writes 8 rows x 128 contiguous bytes.
+__device__ __forceinline__ void quad_store(uint32_t (&v)[4][8], uint8_t* base, int64_t row0,
+                                           int64_t stride, int q_row0, int n_valid) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, p = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    if (q_row0 + 4 * g + r < n_valid)
+      st_global_v8_b32(base + (row0 + 4 * g + r) * stride + 32 * p, v[r]);
+}
+
+// grouped_gemm_kernel<true>, where every CTA takes whole tiles: two epilogue sets,
+// warps 2..5 (set 0) and 10..13 (set 1), each one warp per TMEM lane
+// quarter, take half of every tile's output columns (L1: h columns
+// [64 set, 64 set + 64), from gate columns 64 set + c and up columns
+// 128 + 64 set + c; L2: columns [128 set, 128 set + 128)).  The arithmetic
+// is epi_l1's and epi_l2's; without taps the rows are regrouped by
+// quad_transpose and stored 128 bytes per row piece (the row-per-lane stores
+// of the tapped path make 32 separate 32-byte requests per instruction).
+// acc_empty counts the 8 warps.
 __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Tables& tb,
                                   Barriers* bars, uint32_t tmem, volatile int* abort,
                                   float& amax) {
@@ -981,6 +1022,7 @@ __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Table
   const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
   const float* gs_b_up = args.gs_b_up != nullptr ? args.gs_b_up : args.gs_b;
   const bool mid_alpha = args.mode == 2 && args.gs_mid != nullptr;
+  const bool grouped = args.tap == nullptr;
   WorkIter it;
   it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
   uint32_t acc_phase = 0;
@@ -992,19 +1034,38 @@ __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Table
     const float alpha_u = __fmul_rn(gs_m, __ldg(gs_b_up + ti.e));
     if (!mbar_wait(&bars->acc_full, acc_phase, args.status, abort)) return false;
     tc_fence_after();
-    const bool valid = ti.mt * kBM + row_in_tile < tb.cnt[ti.e];
-    const int64_t row = tb.off[ti.e] + ti.mt * kBM + row_in_tile;
-    const int nv_w = min(32, max(0, tb.cnt[ti.e] - ti.mt * kBM - q * 32));
+    const int n_valid = tb.cnt[ti.e] - ti.mt * kBM;          // valid rows of the tile
+    const bool valid = row_in_tile < n_valid;
+    const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
+    const int64_t row = row0 + row_in_tile;
+    const int nv_w = min(32, max(0, n_valid - q * 32));
     if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
       // few rows: each row's columns spread over the lanes, as in epi_l1_1
-      const int64_t qrow0 = tb.off[ti.e] + ti.mt * kBM + q * 32;
       for (int c = 0; c < 2; ++c) {
         float g[32], u[32];
         tmem_ld_f32(t_row + set * 64 + c * 32, g);
         tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
         for (int r = 0; r < nv_w; ++r)
-          epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u, qrow0 + r,
-                   ti.nt * 128 + set * 64 + c * 32 + lane, args, amax);
+          epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u,
+                   row0 + q * 32 + r, ti.nt * 128 + set * 64 + c * 32 + lane, args, amax);
+      }
+    } else if (args.mode == 1 && nv_w > 0 && grouped) {
+      uint8_t* base = reinterpret_cast<uint8_t*>(args.out) +
+                      (ti.nt * 128 + set * 64) * sizeof(float);
+      for (int c = 0; c < 2; ++c) {
+        float g[32], u[32];
+        tmem_ld_f32(t_row + set * 64 + c * 32, g);
+        tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
+        uint32_t v[4][8];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float h = __fmul_rn(silu_f(__fmul_rn(alpha, g[j])), __fmul_rn(alpha_u, u[j]));
+          if (valid) amax = fmaxf(amax, fabsf(h));
+          v[j / 8][j % 8] = __float_as_uint(h);
+        }
+        quad_transpose(v);
+        quad_store(v, base + c * 32 * sizeof(float), row0 + q * 32,
+                   static_cast<int64_t>(args.I) * sizeof(float), q * 32, n_valid);
       }
     } else if (args.mode == 1 && nv_w > 0) {
       for (int c = 0; c < 2; ++c) {
@@ -1013,7 +1074,42 @@ __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Table
         tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
         if (valid) epi_l1(g, u, alpha, alpha_u, row, ti.nt * 128 + set * 64 + c * 32, args, amax);
       }
-    } else if (args.mode != 1 && nv_w > 0) {
+    } else if (args.mode != 1 && nv_w > 0 && grouped && args.out_dtype != 1) {
+      // 16-bit slot rows: 64 columns (128 bytes) per round
+      const bool half = args.out_dtype == 2;
+      uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (ti.nt * kBN + set * 128) * 2;
+      float big = 0.0f;
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[4][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float a[32];
+          tmem_ld_f32(t_row + set * 128 + c * 64 + h * 32, a);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float x0 = __fmul_rn(alpha, a[2 * j]), x1 = __fmul_rn(alpha, a[2 * j + 1]);
+            big = fmaxf(big, fmaxf(fabsf(x0), fabsf(x1)));
+            v[2 * h + j / 8][j % 8] = half ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
+          }
+        }
+        quad_transpose(v);
+        quad_store(v, base + c * 64 * 2, row0 + q * 32, static_cast<int64_t>(args.N) * 2, q * 32,
+                   n_valid);
+      }
+      if (half && valid && !(big <= kF16Max)) record_status(args.status, kErrRange);
+    } else if (args.mode != 1 && nv_w > 0 && grouped) {
+      uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (ti.nt * kBN + set * 128) * 4;
+      for (int c = 0; c < 4; ++c) {
+        float a[32];
+        tmem_ld_f32(t_row + set * 128 + c * 32, a);
+        uint32_t v[4][8];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j / 8][j % 8] = __float_as_uint(__fmul_rn(alpha, a[j]));
+        quad_transpose(v);
+        quad_store(v, base + c * 32 * 4, row0 + q * 32, static_cast<int64_t>(args.N) * 4, q * 32,
+                   n_valid);
+      }
+    } else if (nv_w > 0) {
       for (int c = 0; c < 4; ++c) {
         float a[32];
         tmem_ld_f32(t_row + set * 128 + c * 32, a);

@@ -394,6 +394,14 @@ __device__ __forceinline__ uint64_t clock64_now() {
 
 // One 32-byte store of 8 floats (p 32-byte aligned): a whole L2 sector per
 // thread instead of two half-sector writes.
+// Eight 32-bit words (32 bytes, 32-byte aligned address).
+__device__ __forceinline__ void st_global_v8_b32(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                 "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void st_global_v8(float* p, const float (&v)[8]) {
   asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),

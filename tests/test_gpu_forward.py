@@ -204,6 +204,37 @@ def test_paths_agree_bit_for_bit(nb, name):
     assert np.array_equal(a["y"], b["y"])
 
 
+@pytest.mark.parametrize("slot_dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+def test_untapped_matches_tapped(nb, slot_dtype):
+    """Without taps the whole-tile GEMM hands the accumulator back before
+    its global stores (h and 16-bit slot rows held in registers); with taps it
+    stores first.  Same arithmetic, so the slot rows and y are identical.  The
+    waves workload has enough tiles for the whole-tile kernel on both GEMMs."""
+    cfg = syn.CONFIGS["waves"]
+    x = syn.draw_activations(cfg).to(DEV)
+    ids, w = syn.draw_routing(cfg)
+    ids, w = ids.to(DEV), w.to(DEV)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)]).to(DEV)
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)]).to(DEV)
+    q1, s1, g1 = nb.quantize_weights(W1)
+    q2, s2, g2 = nb.quantize_weights(W2)
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    outs = []
+    for tapped in (False, True):
+        layer = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, slot_dtype=slot_dtype)
+        taps = {"path": 1}
+        if tapped:
+            taps["l1_out"] = torch.zeros((layer.rows, 2 * cfg.I), dtype=torch.float32, device=DEV)
+        y = layer.forward(x, ids, w, taps=taps)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        rows = layer.route.slot_of[:cfg.T * cfg.k].long()
+        outs.append((y.float().cpu(), layer.slot_out[rows].float().cpu()))
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][0], outs[1][0])
+
+
 def test_forward_bf16_output(nb):
     cfg = syn.CONFIGS["small"]
     x = syn.draw_activations(cfg)
