@@ -303,10 +303,15 @@ typedef struct {
  *            [3] after the L2 GEMM (all four or none; on the fused path
  *            [1..3] are all recorded after the single kernel).
  *   path     NVMOE_PATH_AUTO (0, default), NVMOE_PATH_SEPARATE (three
- *            launches: L1, requantisation, L2) or NVMOE_PATH_FUSED (one
- *            cooperative kernel with two grid barriers).  AUTO takes the
- *            fused kernel when both GEMMs have fewer than 4 tiles per SM.
- *            Both paths compute identical results.
+ *            launches: L1, requantisation, L2), NVMOE_PATH_FUSED (one
+ *            cooperative kernel with two grid barriers) or
+ *            NVMOE_PATH_SEPARATE_SINGLE (three launches, every GEMM on
+ *            one-CTA tiles).  AUTO takes the fused kernel when both GEMMs
+ *            have fewer than 4 tiles per SM.  On the three-launch path a
+ *            GEMM with at least 4 tiles per SM whatever the routing runs on
+ *            clusters of two CTAs (one tcgen05 MMA over both SMs, M = 256),
+ *            unless SEPARATE_SINGLE.  Every path computes identical
+ *            results.
  * rows = moe_route_rows_bound(T, k, E); padding rows are unspecified.
  * When h / hq / hsf_mma / gs_h are given they replace the workspace buffers
  * of the same name (no extra traffic); l1_out costs one extra store. */
@@ -314,6 +319,7 @@ typedef struct {
 #define NVMOE_PATH_SEPARATE 1
 #define NVMOE_PATH_FUSED 2
 #define NVMOE_PATH_LAYER 3     /* moe_nvfp4_layer_forward only */
+#define NVMOE_PATH_SEPARATE_SINGLE 4
 typedef struct {
   float* l1_out;
   float* h;

@@ -48,7 +48,7 @@ class Taps(ctypes.Structure):
                 ("ready_value", ctypes.c_int), ("ready_wait_us", ctypes.c_int)]
 
 
-PATH_AUTO, PATH_SEPARATE, PATH_FUSED, PATH_LAYER = 0, 1, 2, 3
+PATH_AUTO, PATH_SEPARATE, PATH_FUSED, PATH_LAYER, PATH_SEPARATE_SINGLE = 0, 1, 2, 3, 4
 
 
 # name -> (restype, argtypes)

@@ -390,8 +390,10 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   int path = NVMOE_PATH_AUTO;
   if (taps != nullptr) path = taps->path;
   if (path != NVMOE_PATH_AUTO && path != NVMOE_PATH_SEPARATE && path != NVMOE_PATH_FUSED &&
-      path != NVMOE_PATH_LAYER)
+      path != NVMOE_PATH_LAYER && path != NVMOE_PATH_SEPARATE_SINGLE)
     return NVMOE_ERR_INVALID_ARG;
+  const bool allow_pair = path != NVMOE_PATH_SEPARATE_SINGLE;
+  if (path == NVMOE_PATH_SEPARATE_SINGLE) path = NVMOE_PATH_SEPARATE;
   if (T == 0) return NVMOE_OK;
   FwdBuffers b;
   forward_layout(T, k, E, I, static_cast<uint8_t*>(ws), &b);
@@ -519,7 +521,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
     return NVMOE_OK;
   }
   const int g1 = grid_for(tiles1);
-  cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, mt_min * a1.n_tiles, stream), 1);
+  cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, mt_min * a1.n_tiles, allow_pair, stream), 1);
   if (e != cudaSuccess) return fail(e);
   if (timed && note(cudaEventRecord(ev[1], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
   if (w->gs_mid == nullptr) {
@@ -530,7 +532,8 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
     if (e != cudaSuccess) return fail(e);
   }
   if (timed && note(cudaEventRecord(ev[2], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
-  e = counted(launch_gemm(a2, map_h, map_w2, grid_for(tiles2), mt_min * a2.n_tiles, stream), 1);
+  e = counted(launch_gemm(a2, map_h, map_w2, grid_for(tiles2), mt_min * a2.n_tiles, allow_pair,
+                                  stream), 1);
   if (e != cudaSuccess) return fail(e);
   if (timed && note(cudaEventRecord(ev[3], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
   return NVMOE_OK;

@@ -668,7 +668,6 @@ __device__ __forceinline__ void write_stage_sf(int stage, Barriers* bars, const 
 __device__ bool run_sf_writer(const Phase& P, Barriers* bars, uint8_t* smem, uint32_t tmem,
                               Pipe& pp, volatile int* abort) {
   const GemmArgs& args = *P.a;
-  const int lane = threadIdx.x & 31;
   const uint32_t q = (threadIdx.x >> 5) & 3;
   const uint32_t lane_base = tmem + ((q * 32u) << 16);
   WorkIter it;
@@ -1011,18 +1010,106 @@ __device__ __forceinline__ void quad_store(uint32_t (&v)[4][8], uint8_t* base, i
 // quad_transpose and stored 128 bytes per row piece (the row-per-lane stores
 // of the tapped path make 32 separate 32-byte requests per instruction).
 // acc_empty counts the 8 warps.
+// One tile's share of an epilogue set (see run_epilogue_half): rows
+// row0 + [0, 128) of which n_valid are valid, output column tile nt; this
+// warp's TMEM lanes at t_row.
+__device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int n_valid,
+                                              int64_t row0, float alpha, float alpha_u,
+                                              uint32_t t_row, int set, float& amax) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int row_in_tile = q * 32 + lane;
+  const bool grouped = args.tap == nullptr;
+  const bool valid = row_in_tile < n_valid;
+  const int64_t row = row0 + row_in_tile;
+  const int nv_w = min(32, max(0, n_valid - q * 32));
+  if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
+    // few rows: each row's columns spread over the lanes, as in epi_l1_1
+    for (int c = 0; c < 2; ++c) {
+      float g[32], u[32];
+      tmem_ld_f32(t_row + set * 64 + c * 32, g);
+      tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
+      for (int r = 0; r < nv_w; ++r)
+        epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u,
+                 row0 + q * 32 + r, nt * 128 + set * 64 + c * 32 + lane, args, amax);
+    }
+  } else if (args.mode == 1 && nv_w > 0 && grouped) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * 128 + set * 64) * sizeof(float);
+    for (int c = 0; c < 2; ++c) {
+      float g[32], u[32];
+      tmem_ld_f32(t_row + set * 64 + c * 32, g);
+      tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
+      uint32_t v[4][8];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float h = __fmul_rn(silu_f(__fmul_rn(alpha, g[j])), __fmul_rn(alpha_u, u[j]));
+        if (valid) amax = fmaxf(amax, fabsf(h));
+        v[j / 8][j % 8] = __float_as_uint(h);
+      }
+      quad_transpose(v);
+      quad_store(v, base + c * 32 * sizeof(float), row0 + q * 32,
+                 static_cast<int64_t>(args.I) * sizeof(float), q * 32, n_valid);
+    }
+  } else if (args.mode == 1 && nv_w > 0) {
+    for (int c = 0; c < 2; ++c) {
+      float g[32], u[32];
+      tmem_ld_f32(t_row + set * 64 + c * 32, g);
+      tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
+      if (valid) epi_l1(g, u, alpha, alpha_u, row, nt * 128 + set * 64 + c * 32, args, amax);
+    }
+  } else if (args.mode != 1 && nv_w > 0 && grouped && args.out_dtype != 1) {
+    // 16-bit slot rows: 64 columns (128 bytes) per round
+    const bool half = args.out_dtype == 2;
+    uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * kBN + set * 128) * 2;
+    float big = 0.0f;
+    for (int c = 0; c < 2; ++c) {
+      uint32_t v[4][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float a[32];
+        tmem_ld_f32(t_row + set * 128 + c * 64 + h * 32, a);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x0 = __fmul_rn(alpha, a[2 * j]), x1 = __fmul_rn(alpha, a[2 * j + 1]);
+          big = fmaxf(big, fmaxf(fabsf(x0), fabsf(x1)));
+          v[2 * h + j / 8][j % 8] = half ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
+        }
+      }
+      quad_transpose(v);
+      quad_store(v, base + c * 64 * 2, row0 + q * 32, static_cast<int64_t>(args.N) * 2, q * 32,
+                 n_valid);
+    }
+    if (half && valid && !(big <= kF16Max)) record_status(args.status, kErrRange);
+  } else if (args.mode != 1 && nv_w > 0 && grouped) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * kBN + set * 128) * 4;
+    for (int c = 0; c < 4; ++c) {
+      float a[32];
+      tmem_ld_f32(t_row + set * 128 + c * 32, a);
+      uint32_t v[4][8];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j / 8][j % 8] = __float_as_uint(__fmul_rn(alpha, a[j]));
+      quad_transpose(v);
+      quad_store(v, base + c * 32 * 4, row0 + q * 32, static_cast<int64_t>(args.N) * 4, q * 32,
+                 n_valid);
+    }
+  } else if (nv_w > 0) {
+    for (int c = 0; c < 4; ++c) {
+      float a[32];
+      tmem_ld_f32(t_row + set * 128 + c * 32, a);
+      if (valid) epi_l2(a, alpha, row, nt * kBN + set * 128 + c * 32, args);
+    }
+  }
+}
+
 __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Tables& tb,
                                   Barriers* bars, uint32_t tmem, volatile int* abort,
                                   float& amax) {
   const GemmArgs& args = *P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;
   const int set = warp >= kEpi2Warp0 ? 1 : 0;
-  const int row_in_tile = q * 32 + lane;
-  const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const float* gs_b_up = args.gs_b_up != nullptr ? args.gs_b_up : args.gs_b;
   const bool mid_alpha = args.mode == 2 && args.gs_mid != nullptr;
-  const bool grouped = args.tap == nullptr;
   WorkIter it;
   it.init(P.total_tiles, P.k_stages, gridDim.x, blockIdx.x, P.whole_tiles);
   uint32_t acc_phase = 0;
@@ -1034,88 +1121,8 @@ __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Table
     const float alpha_u = __fmul_rn(gs_m, __ldg(gs_b_up + ti.e));
     if (!mbar_wait(&bars->acc_full, acc_phase, args.status, abort)) return false;
     tc_fence_after();
-    const int n_valid = tb.cnt[ti.e] - ti.mt * kBM;          // valid rows of the tile
-    const bool valid = row_in_tile < n_valid;
-    const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
-    const int64_t row = row0 + row_in_tile;
-    const int nv_w = min(32, max(0, n_valid - q * 32));
-    if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
-      // few rows: each row's columns spread over the lanes, as in epi_l1_1
-      for (int c = 0; c < 2; ++c) {
-        float g[32], u[32];
-        tmem_ld_f32(t_row + set * 64 + c * 32, g);
-        tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
-        for (int r = 0; r < nv_w; ++r)
-          epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u,
-                   row0 + q * 32 + r, ti.nt * 128 + set * 64 + c * 32 + lane, args, amax);
-      }
-    } else if (args.mode == 1 && nv_w > 0 && grouped) {
-      uint8_t* base = reinterpret_cast<uint8_t*>(args.out) +
-                      (ti.nt * 128 + set * 64) * sizeof(float);
-      for (int c = 0; c < 2; ++c) {
-        float g[32], u[32];
-        tmem_ld_f32(t_row + set * 64 + c * 32, g);
-        tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
-        uint32_t v[4][8];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float h = __fmul_rn(silu_f(__fmul_rn(alpha, g[j])), __fmul_rn(alpha_u, u[j]));
-          if (valid) amax = fmaxf(amax, fabsf(h));
-          v[j / 8][j % 8] = __float_as_uint(h);
-        }
-        quad_transpose(v);
-        quad_store(v, base + c * 32 * sizeof(float), row0 + q * 32,
-                   static_cast<int64_t>(args.I) * sizeof(float), q * 32, n_valid);
-      }
-    } else if (args.mode == 1 && nv_w > 0) {
-      for (int c = 0; c < 2; ++c) {
-        float g[32], u[32];
-        tmem_ld_f32(t_row + set * 64 + c * 32, g);
-        tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
-        if (valid) epi_l1(g, u, alpha, alpha_u, row, ti.nt * 128 + set * 64 + c * 32, args, amax);
-      }
-    } else if (args.mode != 1 && nv_w > 0 && grouped && args.out_dtype != 1) {
-      // 16-bit slot rows: 64 columns (128 bytes) per round
-      const bool half = args.out_dtype == 2;
-      uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (ti.nt * kBN + set * 128) * 2;
-      float big = 0.0f;
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[4][8];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float a[32];
-          tmem_ld_f32(t_row + set * 128 + c * 64 + h * 32, a);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float x0 = __fmul_rn(alpha, a[2 * j]), x1 = __fmul_rn(alpha, a[2 * j + 1]);
-            big = fmaxf(big, fmaxf(fabsf(x0), fabsf(x1)));
-            v[2 * h + j / 8][j % 8] = half ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
-          }
-        }
-        quad_transpose(v);
-        quad_store(v, base + c * 64 * 2, row0 + q * 32, static_cast<int64_t>(args.N) * 2, q * 32,
-                   n_valid);
-      }
-      if (half && valid && !(big <= kF16Max)) record_status(args.status, kErrRange);
-    } else if (args.mode != 1 && nv_w > 0 && grouped) {
-      uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (ti.nt * kBN + set * 128) * 4;
-      for (int c = 0; c < 4; ++c) {
-        float a[32];
-        tmem_ld_f32(t_row + set * 128 + c * 32, a);
-        uint32_t v[4][8];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j / 8][j % 8] = __float_as_uint(__fmul_rn(alpha, a[j]));
-        quad_transpose(v);
-        quad_store(v, base + c * 32 * 4, row0 + q * 32, static_cast<int64_t>(args.N) * 4, q * 32,
-                   n_valid);
-      }
-    } else if (nv_w > 0) {
-      for (int c = 0; c < 4; ++c) {
-        float a[32];
-        tmem_ld_f32(t_row + set * 128 + c * 32, a);
-        if (valid) epi_l2(a, alpha, row, ti.nt * kBN + set * 128 + c * 32, args);
-      }
-    }
+    epi_tile_half(args, ti.nt, tb.cnt[ti.e] - ti.mt * kBM, tb.off[ti.e] + ti.mt * kBM, alpha,
+                  alpha_u, t_row, set, amax);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->acc_empty);
@@ -1265,6 +1272,334 @@ __global__ void __launch_bounds__(kHalf ? kThreadsHalf : kThreadsSt, 1) grouped_
     if (args.mode == 1) publish_amax(amax, s_amax, args.amax_partial);
   }
   teardown_cta(bars, tmem);
+}
+
+// ----------------------------------------------------------- CTA pairs --
+// grouped_gemm_pair_kernel: the whole-tile GEMM over clusters of two CTAs.
+// One MMA (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 64), issued by
+// the even CTA, computes two m-tiles of one expert against one 256-row B
+// tile: CTA r holds its own m-tile of A (128 rows) and B rows
+// [128 r, 128 r + 128) of the tile in its shared memory, and its 128 x 256
+// accumulator in its TMEM.  Halving B per CTA halves the B traffic into
+// each SM and makes a stage 38 KB, so five stages fit where a one-CTA tile
+// holds four.  Each CTA loads its own operands, its own A scales and all
+// 256 rows of B scales (its TMEM gets the scale layout of the one-CTA
+// kernel); its four scale writers arrive on the even CTA's sf_full, which
+// therefore means "both CTAs' loads have landed and both CTAs' scales are in
+// TMEM" and is the one barrier the MMA thread waits for.  The MMA thread's
+// commits arrive on the stage's empty barrier and on acc_full in both CTAs;
+// both CTAs' epilogue warps (8 each) arrive on the even CTA's acc_empty.
+// Pair tiles are (expert, n-tile, m-tile pair); an expert with an odd
+// number of m-tiles leaves the odd CTA of its last pair without rows: it
+// loads the even CTA's m-tile again (always in bounds) and stores nothing.
+constexpr int kStagesP = 5;
+constexpr int kBHalfBytes = 128 * kRowBytes;                             // 16384
+constexpr uint32_t kStageTxP = kABytes + kBHalfBytes + kSfaBytes + kSfbBytes;
+constexpr int kOffAP = 0;
+constexpr int kOffBP = kOffAP + kStagesP * kABytes;
+constexpr int kOffSfaP = kOffBP + kStagesP * kBHalfBytes;
+constexpr int kOffSfbP = kOffSfaP + kStagesP * kSfaBytes;
+constexpr int kOffBarP = kOffSfbP + kStagesP * kSfbBytes;
+constexpr int kSmemBytesP = kOffBarP + 256 + 1024;
+// TMEM: accumulator columns [0, 256); B scales 32 columns per stage from
+// 256, A scales 16 per stage from 416 (every tcgen05.st at a multiple of its
+// width; MMA scale addresses at multiples of 8 and 4)
+constexpr uint32_t kTmemSfbP = 256;
+constexpr uint32_t kTmemSfaP = kTmemSfbP + kStagesP * 32;
+static_assert(kTmemSfaP + kStagesP * 16 <= kTmemCols, "pair TMEM columns");
+
+struct BarriersP {
+  uint64_t full[kStagesP];      // this CTA's loads of the stage
+  uint64_t empty[kStagesP];     // the pair's MMAs on the stage are done
+  uint64_t sf_full[kStagesP];   // even CTA: both CTAs' scales written (8 warps)
+  uint64_t acc_full;            // the tile's MMAs are done
+  uint64_t acc_empty;           // even CTA: both CTAs' epilogues released (16 warps)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(BarriersP) <= 256, "pair barriers");
+
+struct PairTables {
+  int prefix[kMaxExperts + 1];  // pair-tile prefix
+  int pmt[kMaxExperts];         // m-tile pairs per expert
+  int mtiles[kMaxExperts];
+  int off[kMaxExperts];
+  int cnt[kMaxExperts];
+};
+
+__device__ void load_pair_tables(PairTables& tb, const GemmArgs& a) {
+  const int E = a.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = a.expert_counts[e];
+    tb.cnt[e] = c;
+    tb.off[e] = a.expert_offsets[e];
+    tb.mtiles[e] = (c + kBM - 1) / kBM;
+    tb.pmt[e] = (tb.mtiles[e] + 1) / 2;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int p = 0;
+    for (int e = 0; e < E; ++e) {
+      tb.prefix[e] = p;
+      p += tb.pmt[e] * a.n_tiles;
+    }
+    tb.prefix[E] = p;
+  }
+  __syncthreads();
+}
+
+// This CTA's m-tile of pair tile t and whether it holds rows.
+struct PairTile {
+  int e, nt, m;
+  bool has_rows;
+};
+
+__device__ __forceinline__ PairTile pair_tile(int t, const PairTables& tb, int E, uint32_t rank) {
+  const TileInfo ti = decode_tile(t, tb.prefix, tb.pmt, E);
+  PairTile p;
+  p.e = ti.e;
+  p.nt = ti.nt;
+  p.m = 2 * ti.mt + static_cast<int>(rank);
+  p.has_rows = p.m < tb.mtiles[ti.e];
+  return p;
+}
+
+__device__ bool run_producer_pair(const GemmArgs& args, const PairTables& tb, const AMaps* map_a,
+                                  const CUtensorMap* map_b, BarriersP* bars, uint8_t* smem,
+                                  uint32_t rank, volatile int* abort, int& issued, int& stage,
+                                  uint32_t& phase) {
+  const int E = args.E;
+  const int k_stages = (args.K + kStageK - 1) / kStageK;
+  const int k_atoms = k_stages * 4;
+  const uint64_t pol_a = policy_evict_last();
+  const uint64_t pol_b = policy_evict_first();
+  if (args.ready_flag != nullptr &&
+      !wait_flag(args.ready_flag, args.ready_value, args.status, abort, args.ready_limit_ns))
+    return false;
+  const int n_clusters = gridDim.x >> 1;
+  for (int t = blockIdx.x >> 1; t < tb.prefix[E]; t += n_clusters) {
+    const PairTile pt = pair_tile(t, tb, E, rank);
+    const int m = pt.has_rows ? pt.m : pt.m - 1;            // the even CTA's m-tile
+    const int a_row = tb.off[pt.e] + m * kBM;
+    int b_row0, b_row1;
+    if (args.mode == 1) {
+      b_row0 = pt.e * args.N + pt.nt * 128;
+      b_row1 = b_row0 + args.I;
+    } else {
+      b_row0 = pt.e * args.N + pt.nt * kBN;
+      b_row1 = b_row0 + 128;
+    }
+    const int b_tile = ((rank == 0 ? b_row0 : b_row1) / 128) * k_stages;
+    const uint8_t* sfb0 = args.b_sf + (static_cast<size_t>(b_row0 / 128) * k_atoms) * kSfAtomBytes;
+    const uint8_t* sfb1 = args.b_sf + (static_cast<size_t>(b_row1 / 128) * k_atoms) * kSfAtomBytes;
+    const uint8_t* sfa = args.a_sf + (static_cast<size_t>(a_row / 128) * k_atoms) * kSfAtomBytes;
+    for (int ks = 0; ks < k_stages; ++ks) {
+      if (!mbar_wait(&bars->empty[stage], phase ^ 1u, args.status, abort)) return false;
+      uint64_t* full = &bars->full[stage];
+      mbar_arrive_expect_tx(full, kStageTxP);
+      const size_t koff = static_cast<size_t>(ks) * 4 * kSfAtomBytes;
+      tma_load_3d(smem + kOffBP + stage * kBHalfBytes, map_b, 0, 0, b_tile + ks, full, pol_b);
+      bulk_load(smem + kOffSfbP + stage * kSfbBytes, sfb0 + koff, kSfaBytes, full, pol_b);
+      bulk_load(smem + kOffSfbP + stage * kSfbBytes + kSfaBytes, sfb1 + koff, kSfaBytes, full,
+                pol_b);
+      tma_load_2d(smem + kOffAP + stage * kABytes, &map_a->full, ks * kRowBytes, a_row, full,
+                  pol_a);
+      bulk_load(smem + kOffSfaP + stage * kSfaBytes, sfa + koff, kSfaBytes, full, pol_a);
+      ++issued;
+      if (++stage == kStagesP) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ bool run_mma_pair(const GemmArgs& args, const PairTables& tb, BarriersP* bars,
+                             uint8_t* smem, uint32_t tmem, volatile int* abort) {
+  const int E = args.E;
+  const int k_stages = (args.K + kStageK - 1) / kStageK;
+  const int k_blocks = args.K / 64;
+  const uint32_t idesc = idesc_mxf4nvf4(2 * kBM, kBN);
+  const int n_clusters = gridDim.x >> 1;
+  int stage = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  for (int t = blockIdx.x >> 1; t < tb.prefix[E]; t += n_clusters) {
+    if (!mbar_wait(&bars->acc_empty, acc_phase ^ 1u, args.status, abort)) return false;
+    tc_fence_after();
+    for (int ks = 0; ks < k_stages; ++ks) {
+      if (!mbar_wait(&bars->sf_full[stage], phase, args.status, abort)) return false;
+      tc_fence_after();
+      const uint32_t sfa_t = tmem + kTmemSfaP + stage * 16;
+      const uint32_t sfb_t = tmem + kTmemSfbP + stage * 32;
+      const uint32_t a_base = smem_u32(smem + kOffAP + stage * kABytes);
+      const uint32_t b_base = smem_u32(smem + kOffBP + stage * kBHalfBytes);
+      const int nkb = min(4, k_blocks - ks * 4);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const uint64_t adesc = smem_desc(a_base + kb * 32, 16, 1024, 2);
+        const uint64_t bdesc = smem_desc(b_base + kb * 32, 16, 1024, 2);
+        mma_mxf4nvf4_pair(tmem, adesc, bdesc, idesc, sfa_t + kb * 4, sfb_t + kb * 8,
+                          (ks != 0 || kb != 0) ? 1u : 0u);
+      }
+      tc_commit_pair(&bars->empty[stage], 3);
+      if (++stage == kStagesP) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    tc_commit_pair(&bars->acc_full, 3);
+    acc_phase ^= 1u;
+  }
+  return true;
+}
+
+// Scale writers of a pair CTA: as run_sf_writer, into this CTA's TMEM, then
+// an arrival on the even CTA's sf_full.
+__device__ bool run_sf_writer_pair(const GemmArgs& args, const PairTables& tb, BarriersP* bars,
+                                   const uint8_t* smem, uint32_t tmem, volatile int* abort) {
+  const int E = args.E;
+  const int lane = threadIdx.x & 31;
+  const uint32_t q = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_base = tmem + ((q * 32u) << 16);
+  const int k_stages = (args.K + kStageK - 1) / kStageK;
+  const int n_clusters = gridDim.x >> 1;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int t = blockIdx.x >> 1; t < tb.prefix[E]; t += n_clusters) {
+    for (int ks = 0; ks < k_stages; ++ks) {
+      if (!mbar_wait(&bars->full[stage], phase, args.status, abort)) return false;
+      const uint4* sa = reinterpret_cast<const uint4*>(smem + kOffSfaP + stage * kSfaBytes) + lane;
+      const uint4* sb = reinterpret_cast<const uint4*>(smem + kOffSfbP + stage * kSfbBytes) + lane;
+      uint32_t a[16], b[32];
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint4 v = sa[kb * 32];
+        a[4 * kb] = v.x; a[4 * kb + 1] = v.y; a[4 * kb + 2] = v.z; a[4 * kb + 3] = v.w;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 u = sb[h * 128 + kb * 32];
+          b[8 * kb + 4 * h] = u.x; b[8 * kb + 4 * h + 1] = u.y;
+          b[8 * kb + 4 * h + 2] = u.z; b[8 * kb + 4 * h + 3] = u.w;
+        }
+      }
+      tmem_st_32x32b_x32(lane_base + kTmemSfbP + stage * 32, b);
+      tmem_st_32x32b_x16(lane_base + kTmemSfaP + stage * 16, a);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_shared_rank(smem_u32(&bars->sf_full[stage]), 0));
+      if (++stage == kStagesP) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ bool run_epilogue_pair(const GemmArgs& args, const PairTables& tb, BarriersP* bars,
+                                  uint32_t tmem, uint32_t rank, volatile int* abort,
+                                  float& amax) {
+  const int E = args.E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int set = warp >= kEpi2Warp0 ? 1 : 0;
+  const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const float gs_a = __ldcg(args.gs_a);
+  const float* gs_b_up = args.gs_b_up != nullptr ? args.gs_b_up : args.gs_b;
+  const bool mid_alpha = args.mode == 2 && args.gs_mid != nullptr;
+  const uint32_t acc_empty0 = map_shared_rank(smem_u32(&bars->acc_empty), 0);
+  const int n_clusters = gridDim.x >> 1;
+  uint32_t acc_phase = 0;
+  for (int t = blockIdx.x >> 1; t < tb.prefix[E]; t += n_clusters) {
+    const PairTile pt = pair_tile(t, tb, E, rank);
+    const float gs_m = mid_alpha ? __ldg(args.gs_mid + pt.e) : gs_a;
+    const float alpha = __fmul_rn(gs_m, __ldg(args.gs_b + pt.e));
+    const float alpha_u = __fmul_rn(gs_m, __ldg(gs_b_up + pt.e));
+    if (!mbar_wait(&bars->acc_full, acc_phase, args.status, abort)) return false;
+    tc_fence_after();
+    const int n_valid = pt.has_rows ? tb.cnt[pt.e] - pt.m * kBM : 0;
+    epi_tile_half(args, pt.nt, n_valid, tb.off[pt.e] + pt.m * kBM, alpha, alpha_u, t_row, set,
+                  amax);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(acc_empty0);
+    acc_phase ^= 1u;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreadsHalf, 1) grouped_gemm_pair_kernel(
+    const __grid_constant__ AMaps map_a, const __grid_constant__ CUtensorMap map_b,
+    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  BarriersP* bars = reinterpret_cast<BarriersP*>(smem + kOffBarP);
+  __shared__ PairTables tb;
+  __shared__ float s_amax[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  load_pair_tables(tb, args);
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStagesP; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->sf_full[s], 8);
+    }
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 16);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbarrier_init();
+    prefetch_tensormap(&map_a.full);
+    prefetch_tensormap(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  // both CTAs' barriers are initialised before any remote arrival
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0, stage = 0;
+      uint32_t phase = 0;
+      run_producer_pair(args, tb, &map_a, &map_b, bars, smem, rank, abort, issued, stage, phase);
+      // no copy into this CTA's shared memory is in flight at exit
+      const int tail = issued < kStagesP ? issued : kStagesP;
+      for (int i = 0; i < tail; ++i) {
+        if (--stage < 0) {
+          stage = kStagesP - 1;
+          phase ^= 1u;
+        }
+        mbar_wait(&bars->full[stage], phase, args.status, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      run_mma_pair(args, tb, bars, smem, tmem, abort);
+      tc_commit_pair(&bars->drain, 1);
+      mbar_wait(&bars->drain, 0, args.status, nullptr);
+    }
+  } else if (warp >= kSfWarp0 && warp < kEpi2Warp0) {
+    run_sf_writer_pair(args, tb, bars, smem, tmem, abort);
+  } else {
+    float amax = 0.0f;
+    run_epilogue_pair(args, tb, bars, tmem, rank, abort, amax);
+    if (args.mode == 1) publish_amax_half(amax, s_amax, args.amax_partial);
+  }
+  // the pair's MMAs read both CTAs' shared memory and TMEM: neither leaves
+  // before both are done
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 struct FusedArgs {
@@ -1795,7 +2130,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   }
 }
 
-PerDeviceOnce g_gemm_attr, g_gemm_half_attr, g_fused_attr, g_layer_attr;
+PerDeviceOnce g_gemm_attr, g_gemm_half_attr, g_gemm_pair_attr, g_fused_attr, g_layer_attr;
 
 }  // namespace
 
@@ -1827,11 +2162,30 @@ cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& ma
 int gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
-                        int grid, int64_t min_tiles, cudaStream_t stream) {
+                        int grid, int64_t min_tiles, bool allow_pair, cudaStream_t stream) {
   // At least kStreamKFactor tiles per CTA whatever the routing, and no
-  // requantisation inside the epilogue: whole tiles and two epilogue sets.
+  // requantisation inside the epilogue: whole tiles and two epilogue sets,
+  // over CTA pairs when the grid holds at least one pair.
   const bool half = min_tiles >= int64_t{kStreamKFactor} * grid &&
                     !(args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue);
+  if (half && allow_pair && grid >= 2) {
+    const cudaError_t err = set_smem_attr_once(
+        g_gemm_pair_attr, reinterpret_cast<const void*>(grouped_gemm_pair_kernel), kSmemBytesP);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid & ~1);
+    cfg.blockDim = dim3(kThreadsHalf);
+    cfg.dynamicSmemBytes = kSmemBytesP;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, map_a, map_b, args);
+  }
   if (half) {
     const cudaError_t err = set_smem_attr_once(
         g_gemm_half_attr, reinterpret_cast<const void*>(grouped_gemm_kernel<true>), kSmemBytes);

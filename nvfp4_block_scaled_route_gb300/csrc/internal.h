@@ -130,9 +130,10 @@ struct AMaps {
 };
 constexpr int kSmallABoxRows = 32;
 // min_tiles: tiles that exist whatever the routing (a lower bound); with at
-// least 4 per CTA the kernel with whole tiles and two epilogue sets runs.
+// least 4 per CTA the kernel with whole tiles and two epilogue sets runs,
+// over CTA pairs (cta_group::2) when allow_pair (grid rounded down to even).
 cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
-                        int grid, int64_t min_tiles, cudaStream_t stream);
+                        int grid, int64_t min_tiles, bool allow_pair, cudaStream_t stream);
 int gemm_smem_bytes();
 // L1 -> grid barrier -> requantise -> grid barrier -> L2 in one cooperative
 // launch (grid <= SM count, one CTA per SM).

@@ -93,6 +93,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// Arrive on the mbarrier at shared::cluster address `cluster_addr` (this
+// CTA's or the peer's, from mapa), with the default semantics (release at
+// CTA scope).  Between the CTAs of a pair this is the hand-over the pair's
+// MMAs need: the arriving warps finish their tcgen05 operations
+// (tcgen05.wait + tcgen05.fence::before_thread_sync) first, and the waiter
+// issues tcgen05.fence::after_thread_sync after its wait.  A release at
+// cluster scope costs the arriving thread about 1.4k cycles per arrival.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // ----------------------------------------------------------------- TMA ----
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map,
                                             int32_t x, int32_t y, uint64_t* bar,

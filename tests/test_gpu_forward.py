@@ -235,6 +235,48 @@ def test_untapped_matches_tapped(nb, slot_dtype):
     assert torch.equal(outs[0][0], outs[1][0])
 
 
+@pytest.mark.parametrize("slot_dtype", [torch.float32, torch.float16], ids=["f32", "f16"])
+@pytest.mark.parametrize("tapped", [False, True], ids=["untapped", "tapped"])
+def test_cta_pair_gemm_matches_one_cta(nb, slot_dtype, tapped):
+    """Enough tiles for the GEMMs over CTA pairs (one MMA across two SMs,
+    M = 256) on the three-launch path: 2473 tokens, top-4 over 8 experts of
+    the waves shapes (H=2048, I=1024), at least 77 m-tiles x 8 n-tiles per
+    GEMM.  The counts give experts 9, 10 and 11 m-tiles, so the last pair of
+    an odd expert has an empty odd CTA.  Forcing one-CTA tiles must give the
+    same bits everywhere."""
+    counts = [1300, 1100, 1290, 1250, 1100, 1300, 1250, 1302]
+    cfg = syn.MoEConfig("pairs", E=8, H=2048, I=1024, T=sum(counts) // 4, k=4,
+                        routing="uniform")
+    x = syn.draw_activations(cfg).to(DEV)
+    ids, w = syn.routing_with_counts(counts, cfg.k)
+    ids, w = ids.to(DEV), w.to(DEV)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)]).to(DEV)
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)]).to(DEV)
+    q1, s1, g1 = nb.quantize_weights(W1)
+    q2, s2, g2 = nb.quantize_weights(W2)
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    counts = torch.bincount(ids.flatten().long(), minlength=cfg.E)
+    assert bool(((counts + 127) // 128 % 2 == 1).any())
+    outs = []
+    for path in (nb.PATH_SEPARATE, nb.PATH_SEPARATE_SINGLE):
+        layer = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, slot_dtype=slot_dtype)
+        taps = {"path": path}
+        if tapped:
+            taps["l1_out"] = torch.zeros((layer.rows, 2 * cfg.I), dtype=torch.float32, device=DEV)
+            taps["h"] = torch.zeros((layer.rows, cfg.I), dtype=torch.float32, device=DEV)
+        y = layer.forward(x, ids, w, taps=taps)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        rows = layer.route.slot_of[:cfg.T * cfg.k].long()
+        got = {"y": y.float().cpu(), "slot": layer.slot_out[rows].float().cpu()}
+        if tapped:
+            got["l1"] = taps["l1_out"][rows].cpu()
+            got["h"] = taps["h"][rows].cpu()
+        outs.append(got)
+    for key in outs[0]:
+        assert torch.equal(outs[0][key], outs[1][key]), key
+
+
 def test_forward_bf16_output(nb):
     cfg = syn.CONFIGS["small"]
     x = syn.draw_activations(cfg)
