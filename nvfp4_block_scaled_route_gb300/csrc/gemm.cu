@@ -1012,10 +1012,15 @@ __device__ __forceinline__ void quad_store(uint32_t (&v)[4][8], uint8_t* base, i
 // acc_empty counts the 8 warps.
 // One tile's share of an epilogue set (see run_epilogue_half): rows
 // row0 + [0, 128) of which n_valid are valid, output column tile nt; this
-// warp's TMEM lanes at t_row.
+// warp's TMEM lanes at t_row.  release() hands the accumulator back: on the
+// untapped paths as soon as this warp's share is in registers (h, or the
+// 16-bit slot rows, regrouped for the stores), so that the stores overlap
+// the next tile's MMAs; elsewhere after the stores.
+template <typename Release>
 __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int n_valid,
                                               int64_t row0, float alpha, float alpha_u,
-                                              uint32_t t_row, int set, float& amax) {
+                                              uint32_t t_row, int set, float& amax,
+                                              Release release) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int row_in_tile = q * 32 + lane;
@@ -1023,7 +1028,9 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
   const bool valid = row_in_tile < n_valid;
   const int64_t row = row0 + row_in_tile;
   const int nv_w = min(32, max(0, n_valid - q * 32));
-  if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
+  if (nv_w == 0) {
+    release();
+  } else if (args.mode == 1 && nv_w <= kNarrowRows) {
     // few rows: each row's columns spread over the lanes, as in epi_l1_1
     for (int c = 0; c < 2; ++c) {
       float g[32], u[32];
@@ -1033,37 +1040,44 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
         epi_l1_1(from_lane_column(g, r), from_lane_column(u, r), alpha, alpha_u,
                  row0 + q * 32 + r, nt * 128 + set * 64 + c * 32 + lane, args, amax);
     }
-  } else if (args.mode == 1 && nv_w > 0 && grouped) {
+    release();
+  } else if (args.mode == 1 && grouped) {
     uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * 128 + set * 64) * sizeof(float);
+    uint32_t v[2][4][8];
+#pragma unroll
     for (int c = 0; c < 2; ++c) {
       float g[32], u[32];
       tmem_ld_f32(t_row + set * 64 + c * 32, g);
       tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
-      uint32_t v[4][8];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float h = __fmul_rn(silu_f(__fmul_rn(alpha, g[j])), __fmul_rn(alpha_u, u[j]));
         if (valid) amax = fmaxf(amax, fabsf(h));
-        v[j / 8][j % 8] = __float_as_uint(h);
+        v[c][j / 8][j % 8] = __float_as_uint(h);
       }
-      quad_transpose(v);
-      quad_store(v, base + c * 32 * sizeof(float), row0 + q * 32,
-                 static_cast<int64_t>(args.I) * sizeof(float), q * 32, n_valid);
+      quad_transpose(v[c]);
     }
-  } else if (args.mode == 1 && nv_w > 0) {
+    release();
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      quad_store(v[c], base + c * 32 * sizeof(float), row0 + q * 32,
+                 static_cast<int64_t>(args.I) * sizeof(float), q * 32, n_valid);
+  } else if (args.mode == 1) {
     for (int c = 0; c < 2; ++c) {
       float g[32], u[32];
       tmem_ld_f32(t_row + set * 64 + c * 32, g);
       tmem_ld_f32(t_row + 128 + set * 64 + c * 32, u);
       if (valid) epi_l1(g, u, alpha, alpha_u, row, nt * 128 + set * 64 + c * 32, args, amax);
     }
-  } else if (args.mode != 1 && nv_w > 0 && grouped && args.out_dtype != 1) {
+    release();
+  } else if (grouped && args.out_dtype != 1) {
     // 16-bit slot rows: 64 columns (128 bytes) per round
     const bool half = args.out_dtype == 2;
     uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * kBN + set * 128) * 2;
     float big = 0.0f;
+    uint32_t v[2][4][8];
+#pragma unroll
     for (int c = 0; c < 2; ++c) {
-      uint32_t v[4][8];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float a[32];
@@ -1072,15 +1086,18 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
         for (int j = 0; j < 16; ++j) {
           const float x0 = __fmul_rn(alpha, a[2 * j]), x1 = __fmul_rn(alpha, a[2 * j + 1]);
           big = fmaxf(big, fmaxf(fabsf(x0), fabsf(x1)));
-          v[2 * h + j / 8][j % 8] = half ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
+          v[c][2 * h + j / 8][j % 8] = half ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
         }
       }
-      quad_transpose(v);
-      quad_store(v, base + c * 64 * 2, row0 + q * 32, static_cast<int64_t>(args.N) * 2, q * 32,
-                 n_valid);
+      quad_transpose(v[c]);
     }
+    release();
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      quad_store(v[c], base + c * 64 * 2, row0 + q * 32, static_cast<int64_t>(args.N) * 2, q * 32,
+                 n_valid);
     if (half && valid && !(big <= kF16Max)) record_status(args.status, kErrRange);
-  } else if (args.mode != 1 && nv_w > 0 && grouped) {
+  } else if (grouped) {
     uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * kBN + set * 128) * 4;
     for (int c = 0; c < 4; ++c) {
       float a[32];
@@ -1092,12 +1109,14 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
       quad_store(v, base + c * 32 * 4, row0 + q * 32, static_cast<int64_t>(args.N) * 4, q * 32,
                  n_valid);
     }
-  } else if (nv_w > 0) {
+    release();
+  } else {
     for (int c = 0; c < 4; ++c) {
       float a[32];
       tmem_ld_f32(t_row + set * 128 + c * 32, a);
       if (valid) epi_l2(a, alpha, row, nt * kBN + set * 128 + c * 32, args);
     }
+    release();
   }
 }
 
@@ -1122,10 +1141,11 @@ __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Table
     if (!mbar_wait(&bars->acc_full, acc_phase, args.status, abort)) return false;
     tc_fence_after();
     epi_tile_half(args, ti.nt, tb.cnt[ti.e] - ti.mt * kBM, tb.off[ti.e] + ti.mt * kBM, alpha,
-                  alpha_u, t_row, set, amax);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->acc_empty);
+                  alpha_u, t_row, set, amax, [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->acc_empty);
+                  });
     acc_phase ^= 1u;
   }
   return true;
@@ -1520,10 +1540,11 @@ __device__ bool run_epilogue_pair(const GemmArgs& args, const PairTables& tb, Ba
     tc_fence_after();
     const int n_valid = pt.has_rows ? tb.cnt[pt.e] - pt.m * kBM : 0;
     epi_tile_half(args, pt.nt, n_valid, tb.off[pt.e] + pt.m * kBM, alpha, alpha_u, t_row, set,
-                  amax);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(acc_empty0);
+                  amax, [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acc_empty0);
+                  });
     acc_phase ^= 1u;
   }
   return true;
