@@ -1014,8 +1014,8 @@ __device__ __forceinline__ void quad_store(uint32_t (&v)[4][8], uint8_t* base, i
 // row0 + [0, 128) of which n_valid are valid, output column tile nt; this
 // warp's TMEM lanes at t_row.  release() hands the accumulator back: on the
 // untapped paths as soon as this warp's share is in registers (h, or the
-// 16-bit slot rows, regrouped for the stores), so that the stores overlap
-// the next tile's MMAs; elsewhere after the stores.
+// 16-bit slot rows), so that the regrouping and the stores overlap the next
+// tile's MMAs; elsewhere after the stores.
 template <typename Release>
 __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int n_valid,
                                               int64_t row0, float alpha, float alpha_u,
@@ -1055,13 +1055,14 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
         if (valid) amax = fmaxf(amax, fabsf(h));
         v[c][j / 8][j % 8] = __float_as_uint(h);
       }
-      quad_transpose(v[c]);
     }
     release();
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < 2; ++c) {
+      quad_transpose(v[c]);
       quad_store(v[c], base + c * 32 * sizeof(float), row0 + q * 32,
                  static_cast<int64_t>(args.I) * sizeof(float), q * 32, n_valid);
+    }
   } else if (args.mode == 1) {
     for (int c = 0; c < 2; ++c) {
       float g[32], u[32];
@@ -1089,13 +1090,14 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
           v[c][2 * h + j / 8][j % 8] = half ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
         }
       }
-      quad_transpose(v[c]);
     }
     release();
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < 2; ++c) {
+      quad_transpose(v[c]);
       quad_store(v[c], base + c * 64 * 2, row0 + q * 32, static_cast<int64_t>(args.N) * 2, q * 32,
                  n_valid);
+    }
     if (half && valid && !(big <= kF16Max)) record_status(args.status, kErrRange);
   } else if (grouped) {
     uint8_t* base = reinterpret_cast<uint8_t*>(args.out) + (nt * kBN + set * 128) * 4;
