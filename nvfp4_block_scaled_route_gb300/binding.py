@@ -452,15 +452,20 @@ class FusedLayer:
         self._w = weights.struct()
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
-                taps: Optional[dict] = None, stream=None) -> torch.Tensor:
+                taps: Optional[dict] = None, stream=None,
+                y: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """y: output [T, H] (default: the layer's own self.y), bf16 or fp32."""
+        y = self.y if y is None else y
         xcode = {torch.bfloat16: BF16, torch.float32: F32}[x.dtype]
-        ycode = {torch.bfloat16: BF16, torch.float32: F32}[self.y.dtype]
+        ycode = {torch.bfloat16: BF16, torch.float32: F32}[y.dtype]
+        if tuple(y.shape) != (self.T, self.w.H):
+            raise ValueError(f"y must be [{self.T}, {self.w.H}]")
         t = _taps(taps)
         _check("moe_nvfp4_layer_forward", lib().moe_nvfp4_layer_forward(
             ctypes.byref(self._w), _ptr(x), xcode, _ptr(topk_ids), _ptr(topk_w), self.T, self.k,
-            _ptr(self.y), ycode, ctypes.byref(t) if t is not None else None, _ptr(self.ws),
+            _ptr(y), ycode, ctypes.byref(t) if t is not None else None, _ptr(self.ws),
             self.ws.numel(), _stream(stream)))
-        return self.y
+        return y
 
     def staging(self, x_dtype=torch.bfloat16):
         """Pinned host buffers for a step's inputs (x, topk_ids, topk_w) in one
@@ -502,3 +507,94 @@ class FusedLayer:
 
     def status(self) -> int:
         return read_status(self.ws)
+
+
+class StagedPipeline:
+    """Steps of a FusedLayer fed from pinned host memory with the copies
+    overlapped: `depth` slots, each a pinned host input block (x, topk_ids,
+    topk_w in one allocation), its device twin, a device y and a pinned host
+    y.  submit() enqueues one step on three streams -- the host-to-device
+    copy of the slot's inputs (copy-in stream), the layer (compute stream),
+    the device-to-host copy of its y (copy-out stream) -- ordered by per-slot
+    events, so that step i's input copy and step i-1's readback overlap the
+    layer of another step.  Every step still moves all of its own inputs in
+    and its own y out.
+
+    Host buffers of a slot may be refilled once input_consumed(slot) has
+    completed, and the slot's host y read once output_ready(slot) has.
+    The layer's workspace is used by one step at a time (compute stream)."""
+
+    def __init__(self, layer: "FusedLayer", depth: int = 2, x_dtype=torch.bfloat16):
+        if depth < 1:
+            raise ValueError("depth must be >= 1")
+        self.layer = layer
+        self.depth = depth
+        T, k, H = layer.T, layer.k, layer.w.H
+        dev = layer.y.device
+        el = torch.tensor([], dtype=x_dtype).element_size()
+        parts = [T * H * el, T * k * 4, T * k * 4]
+        offs, o = [], 0
+        for n in parts:
+            offs.append(o)
+            o += (n + 255) // 256 * 256
+
+        def views(buf):
+            return (buf[offs[0]:offs[0] + parts[0]].view(x_dtype).view(T, H),
+                    buf[offs[1]:offs[1] + parts[1]].view(torch.int32).view(T, k),
+                    buf[offs[2]:offs[2] + parts[2]].view(torch.float32).view(T, k))
+        self.host_in = [torch.empty(max(o, 256), dtype=torch.uint8).pin_memory()
+                        for _ in range(depth)]
+        self.dev_in = [torch.empty(max(o, 256), dtype=torch.uint8, device=dev)
+                       for _ in range(depth)]
+        self.host_views = [views(b) for b in self.host_in]
+        self.dev_views = [views(b) for b in self.dev_in]
+        self.dev_y = [torch.empty_like(layer.y) for _ in range(depth)]
+        self.host_y = [torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
+                       for _ in range(depth)]
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_comp = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(depth)]     # inputs on the device
+        self.ev_comp = [torch.cuda.Event() for _ in range(depth)]   # layer done
+        self.ev_out = [torch.cuda.Event() for _ in range(depth)]    # y on the host
+        self.h2d_bytes = self.host_in[0].numel()
+        self.d2h_bytes = self.host_y[0].numel() * self.host_y[0].element_size()
+        self._n = 0
+
+    def inputs(self, slot: int):
+        """Host views (x, topk_ids, topk_w) of a slot, to be filled."""
+        return self.host_views[slot]
+
+    def output(self, slot: int) -> torch.Tensor:
+        return self.host_y[slot]
+
+    def input_consumed(self, slot: int) -> torch.cuda.Event:
+        return self.ev_in[slot]
+
+    def output_ready(self, slot: int) -> torch.cuda.Event:
+        return self.ev_out[slot]
+
+    def submit(self, slot: Optional[int] = None) -> int:
+        """Enqueue one step on a slot (default: round-robin); returns it."""
+        if slot is None:
+            slot = self._n % self.depth
+        self._n += 1
+        x, ids, w = self.dev_views[slot]
+        with torch.cuda.stream(self.s_in):
+            self.s_in.wait_event(self.ev_comp[slot])        # the slot's last layer read it
+            self.dev_in[slot].copy_(self.host_in[slot], non_blocking=True)
+            self.ev_in[slot].record(self.s_in)
+        with torch.cuda.stream(self.s_comp):
+            self.s_comp.wait_event(self.ev_in[slot])
+            self.s_comp.wait_event(self.ev_out[slot])       # the slot's last y was read out
+            self.layer.forward(x, ids, w, stream=self.s_comp, y=self.dev_y[slot])
+            self.ev_comp[slot].record(self.s_comp)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_comp[slot])
+            self.host_y[slot].copy_(self.dev_y[slot], non_blocking=True)
+            self.ev_out[slot].record(self.s_out)
+        return slot
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.synchronize()

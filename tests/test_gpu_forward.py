@@ -518,6 +518,44 @@ def test_layer_staged_host_step(nb):
     assert torch.equal(out, y_dev)
 
 
+@pytest.mark.parametrize("name", ["small", "waves"])
+def test_staged_pipeline_overlapped_steps(nb, name):
+    """StagedPipeline: two slots with different inputs, seven steps whose
+    copies overlap other steps' layers; every step's host y equals a direct
+    forward() of its own inputs (a missing or misplaced event would let a
+    step read another slot's inputs or y)."""
+    cfg = syn.CONFIGS[name]
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e, device=DEV) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e, device=DEV) for e in range(cfg.E)])
+    q1, s1, g1 = nb.quantize_weights(W1)
+    q2, s2, g2 = nb.quantize_weights(W2)
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    layer = nb.FusedLayer(pw, cfg.T, cfg.k, device=DEV)
+    pipe = nb.StagedPipeline(layer, depth=2)
+    want = []
+    for slot in range(2):
+        x = syn.draw_activations(cfg) * (1.0 + slot)
+        ids, w = syn.draw_routing(cfg)
+        if slot:
+            ids = torch.flip(ids, dims=[1]).contiguous()
+        want.append(layer.forward(x.to(DEV), ids.to(DEV), w.to(DEV)).cpu().clone())
+        hx, hids, hw = pipe.inputs(slot)
+        hx.copy_(x.to(torch.bfloat16))
+        hids.copy_(ids)
+        hw.copy_(w)
+    torch.cuda.synchronize()
+    for i in range(7):
+        slot = pipe.submit()
+        assert slot == i % 2
+        if i >= 5:
+            pipe.output_ready(slot).synchronize()
+            assert torch.equal(pipe.output(slot), want[slot]), (i, slot)
+    pipe.synchronize()
+    assert layer.status() == 0
+    for slot in range(2):
+        assert torch.equal(pipe.output(slot), want[slot])
+
+
 
 # ------------------------------------------ static intermediate scale ----
 
