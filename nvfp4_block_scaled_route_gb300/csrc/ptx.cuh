@@ -161,6 +161,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -405,6 +411,15 @@ __device__ __forceinline__ uint64_t clock64_now() {
 
 // One 32-byte store of 8 floats (p 32-byte aligned): a whole L2 sector per
 // thread instead of two half-sector writes.
+// The same with an L2 eviction policy (createpolicy) for the written lines.
+__device__ __forceinline__ void st_global_v8_b32_hint(void* p, const uint32_t (&v)[8],
+                                                      uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+               ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                 "r"(v[6]), "r"(v[7]), "l"(policy)
+               : "memory");
+}
+
 // Eight 32-bit words (32 bytes, 32-byte aligned address).
 __device__ __forceinline__ void st_global_v8_b32(void* p, const uint32_t (&v)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
