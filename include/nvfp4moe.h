@@ -381,6 +381,107 @@ int moe_nvfp4_forward(const nvmoe_weights* weights, const uint8_t* xq,
                       void* slot_out, int slot_out_dtype, const nvmoe_taps* taps,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_nvfp4_forward_phase — moe_nvfp4_forward in two calls, for callers whose
+ * h spans several processes (expert parallelism): the requantisation's global
+ * scale is gs_h = amax(h)/2688 over ALL of h ("NVFP4 MoE Pipeline" step 4), so
+ * the amax of every process's h must be reduced before any h is requantised.
+ *   phase 1  L1 GEMM + SiLU*up: h into the workspace, and *amax_h (device
+ *            float) = max |h| over this call's valid rows (0 for T == 0).
+ *   phase 2  requantise h with gs_h = *amax_h/2688 (the caller's reduced
+ *            amax: 0 gives gs 1, as for an all-zero tensor), then the L2 GEMM
+ *            into slot_out.
+ * The arguments are those of moe_nvfp4_forward, the same in both calls, with
+ * the same workspace (it carries h between them).  Always the three-launch
+ * path (the fused kernels need the amax inside).  With weights->gs_mid (a
+ * static intermediate scale) phase 1 requantises in the L1 epilogue and phase
+ * 2 runs L2 alone; *amax_h is then unused by phase 2.  With one process,
+ * phase 1 then phase 2 on the same *amax_h equals moe_nvfp4_forward bit for
+ * bit.  Errors as moe_nvfp4_forward; NVMOE_ERR_INVALID_ARG for phase not 1
+ * or 2 or amax_h NULL. */
+int moe_nvfp4_forward_phase(const nvmoe_weights* weights, const uint8_t* xq,
+                            const uint8_t* xsf_mma, const float* gs_x,
+                            const int32_t* expert_offsets, const int32_t* expert_counts,
+                            const int32_t* row_token, int64_t T, int k, void* slot_out,
+                            int slot_out_dtype, int phase, float* amax_h,
+                            const nvmoe_taps* taps, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/* ----------------------------------------------------- expert parallelism --
+ * The pages' 48 experts are one tensor-parallel rank's share of a larger MoE
+ * ("NVFP4 MoE Debug Log (early)", Symptoms: all 8 TP ranks hold the same
+ * weight shapes; Hypotheses section 7, the per-rank table).  Split the E
+ * experts over G processes instead (E % G == 0; process d owns experts
+ * [d*E/G, (d+1)*E/G)), and a token's slot goes to the owner of its expert:
+ *
+ *   every process: amax of its tokens (nvfp4_amax) -> MAX over processes ->
+ *     quantise its tokens once with that amax (nvfp4_quantize_act_amax,
+ *     row_dst NULL: token rows, row-major scales) -> moe_ep_dispatch ->
+ *     all-to-all of the packed rows and their local expert ids (counts from
+ *     send_counts) ->
+ *   owner: moe_route_permute of the received local expert ids (T = rows
+ *     received, k = 1) -> moe_ep_scatter -> moe_nvfp4_forward_phase 1 ->
+ *     MAX of amax_h over processes -> phase 2 -> moe_ep_gather ->
+ *     all-to-all back (the reverse counts) ->
+ *   every process: moe_unpermute_reduce of the returned rows with
+ *     slot_of = send_pos.
+ *
+ * The exchanges are the caller's collectives (NCCL / torch.distributed).
+ * With the tokens split over the processes in order, every expert sees its
+ * slots in the one-process order and the same global scales, so the result
+ * equals the one-process forward of the whole batch bit for bit.  The
+ * library never synchronises with the host: send_counts must be copied out
+ * by the caller to size the exchange. */
+
+/* Max |x| of a [rows, cols] bf16/fp32 matrix into *amax_out (device float;
+ * 0 for rows == 0).  Workspace: nvfp4_quantize_workspace_size(rows, cols).
+ * Errors as nvfp4_quantize_act. */
+int nvfp4_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, float* amax_out,
+               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* nvfp4_quantize_act with the amax given (*amax_in, device float) instead of
+ * computed: gs = amax/2688 written to *gs_out; no workspace.  The same
+ * arguments and results as nvfp4_quantize_act otherwise (its results equal
+ * nvfp4_quantize_act's when *amax_in is the matrix's own amax). */
+int nvfp4_quantize_act_amax(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                            const int32_t* row_dst, int fanout, int64_t out_rows,
+                            const float* amax_in, uint8_t* q, uint8_t* sf_rowmajor,
+                            uint8_t* sf_mma, float* gs_out, cudaStream_t stream);
+
+/* Dispatch of T tokens' k slots to G processes.
+ *   topk_ids  int32 [T, k] global expert ids (an id outside [0, E) is
+ *             recorded as NVMOE_ERR_DEVICE_BAD_INDEX in the workspace status
+ *             and its slot sent nowhere: send_pos -1)
+ *   q_tok     uint8 [T, H/2] E2M1 token rows; sf_tok uint8 [T, H/16]
+ *             row-major E4M3 scales (nvfp4_quantize_act_amax, row_dst NULL)
+ *   send_counts  int32 [G] out: slots for each process
+ *   send_pos  int32 [T*k] out: row of slot t*k+j in send_rows; the rows of
+ *             process d are [sum of counts before d, +counts[d]), in
+ *             ascending t*k+j
+ *   send_rows uint8 [T*k, H/2 + H/16] out: nibbles then scales per row
+ *   send_expert int32 [T*k] out: the row's expert index on its process
+ *   workspace moe_ep_dispatch_workspace_size(T, k, G), status word first.
+ * Limits: E % G == 0, G <= E <= 256, H % 256 == 0.  16-byte alignment of
+ * q_tok, sf_tok, send_rows, workspace. */
+size_t moe_ep_dispatch_workspace_size(int64_t T, int k, int G);
+int moe_ep_dispatch(const int32_t* topk_ids, int64_t T, int k, int E, int G,
+                    const uint8_t* q_tok, const uint8_t* sf_tok, int H, int32_t* send_counts,
+                    int32_t* send_pos, uint8_t* send_rows, int32_t* send_expert,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Received rows (moe_ep_dispatch's row format, n of them) into the slot
+ * layout of moe_nvfp4_forward: row i's nibbles to xq[slot_of[i]] and its
+ * scales to their staged offsets in xsf_mma (nvfp4_sf_mma_bytes(out_rows, H));
+ * slot_of from moe_route_permute of the received expert ids (k = 1); rows
+ * with slot_of < 0 are skipped.  16-byte alignment of recv_rows, xq, xsf_mma. */
+int moe_ep_scatter(const uint8_t* recv_rows, int64_t n, int H, const int32_t* slot_of,
+                   int64_t out_rows, uint8_t* xq, uint8_t* xsf_mma, cudaStream_t stream);
+
+/* out_rows[i] = slot_out[slot_of[i]] for i < n (H elements of slot_out_dtype
+ * per row; a row with slot_of < 0 is zero): the owner's slot outputs in
+ * received order, for the return exchange.  16-byte alignment. */
+int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, const int32_t* slot_of,
+                  int64_t n, void* out_rows, cudaStream_t stream);
+
 /* -------------------------------------------------------- router front end --
  * moe_router_topk — the step before the routing permutation.  The pages keep
  * the router ("gate") weight in BF16 ("NVFP4 MegaMoE Debug Log", Checkpoint

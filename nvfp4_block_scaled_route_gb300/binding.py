@@ -78,6 +78,14 @@ SIGNATURES = {
     "moe_unpermute_reduce": (_I, [_P, _I, _P, _P, _I64, _I, _I64, _P, _I, _P]),
     "moe_router_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_router_topk": (_I, [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "moe_nvfp4_forward_phase": (_I, [ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _I64, _I,
+                                     _P, _I, _I, _P, ctypes.POINTER(Taps), _P, _SZ, _P]),
+    "nvfp4_amax": (_I, [_P, _I, _I64, _I64, _P, _P, _SZ, _P]),
+    "nvfp4_quantize_act_amax": (_I, [_P, _I, _I64, _I64, _P, _I, _I64, _P, _P, _P, _P, _P, _P]),
+    "moe_ep_dispatch_workspace_size": (_SZ, [_I64, _I, _I]),
+    "moe_ep_dispatch": (_I, [_P, _I64, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ep_scatter": (_I, [_P, _I64, _I, _P, _I64, _P, _P, _P]),
+    "moe_ep_gather": (_I, [_P, _I, _I, _P, _I64, _P, _P]),
     "moe_nvfp4_layer_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_nvfp4_layer_forward": (_I, [ctypes.POINTER(Weights), _P, _I, _P, _P, _I64, _I, _P, _I,
                                      ctypes.POINTER(Taps), _P, _SZ, _P]),
@@ -369,6 +377,96 @@ def nvfp4_forward(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Ten
         code, ctypes.byref(t) if t is not None else None, _ptr(ws), ws.numel(),
         _stream(stream)))
     return slot_out
+
+
+def nvfp4_forward_phase(weights: PreparedWeights, xq: torch.Tensor, xsf_mma: torch.Tensor,
+                        gs_x: torch.Tensor, route: Route, phase: int, amax_h: torch.Tensor,
+                        slot_out: torch.Tensor, ws: torch.Tensor, taps: Optional[dict] = None,
+                        stream=None):
+    """moe_nvfp4_forward_phase: phase 1 (L1, *amax_h = max |h|) or 2
+    (requantise with *amax_h, L2 into slot_out); same arguments and ws."""
+    t = _taps(taps)
+    wst = weights.struct()
+    code = {torch.bfloat16: BF16, torch.float32: F32, torch.float16: F16}[slot_out.dtype]
+    _check("moe_nvfp4_forward_phase", lib().moe_nvfp4_forward_phase(
+        ctypes.byref(wst), _ptr(xq), _ptr(xsf_mma), _ptr(gs_x), _ptr(route.expert_offsets),
+        _ptr(route.expert_counts), _ptr(route.row_token), route.T, route.k, _ptr(slot_out),
+        code, phase, _ptr(amax_h), ctypes.byref(t) if t is not None else None, _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return slot_out
+
+
+# ------------------------------------------------------- expert parallel --
+def amax(x: torch.Tensor, ws: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+         stream=None) -> torch.Tensor:
+    """max |x| of a 2-D bf16/fp32 tensor as a float32 [1] device tensor."""
+    assert x.dim() == 2 and x.is_contiguous()
+    rows, cols = x.shape
+    dtype = {torch.bfloat16: BF16, torch.float32: F32}[x.dtype]
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = _workspace(lib().nvfp4_quantize_workspace_size(rows, cols), x.device)
+    _check("nvfp4_amax", lib().nvfp4_amax(_ptr(x), dtype, rows, cols, _ptr(out), _ptr(ws),
+                                          ws.numel(), _stream(stream)))
+    return out
+
+
+def quantize_act_amax(x: torch.Tensor, amax_in: torch.Tensor, row_dst=None, fanout: int = 1,
+                      out_rows: Optional[int] = None, rowmajor_sf: bool = True,
+                      mma_sf: bool = False, stream=None):
+    """quantize_act with the amax given (float32 [1] device tensor)."""
+    assert x.dim() == 2 and x.is_contiguous()
+    rows, cols = x.shape
+    dtype = {torch.bfloat16: BF16, torch.float32: F32}[x.dtype]
+    out_rows = rows if out_rows is None else out_rows
+    dev = x.device
+    q = torch.empty((out_rows, cols // 2), dtype=torch.uint8, device=dev)
+    sf_row = torch.empty((out_rows, cols // 16), dtype=torch.uint8, device=dev) if rowmajor_sf else None
+    sf_mma = torch.zeros(sf_mma_bytes(out_rows, cols), dtype=torch.uint8, device=dev) if mma_sf else None
+    gs = torch.empty(1, dtype=torch.float32, device=dev)
+    _check("nvfp4_quantize_act_amax", lib().nvfp4_quantize_act_amax(
+        _ptr(x), dtype, rows, cols, _ptr(row_dst), fanout, out_rows, _ptr(amax_in), _ptr(q),
+        _ptr(sf_row), _ptr(sf_mma), _ptr(gs), _stream(stream)))
+    return q, sf_row, sf_mma, gs
+
+
+def ep_dispatch(topk_ids: torch.Tensor, E: int, G: int, q_tok: torch.Tensor,
+                sf_tok: torch.Tensor, ws: Optional[torch.Tensor] = None, stream=None):
+    """moe_ep_dispatch -> (send_counts int32 [G], send_pos int32 [T*k],
+    send_rows uint8 [T*k, H/2 + H/16], send_expert int32 [T*k], ws)."""
+    T, k = topk_ids.shape
+    H = q_tok.shape[1] * 2
+    dev = topk_ids.device
+    S = T * k
+    counts = torch.zeros(G, dtype=torch.int32, device=dev)
+    pos = torch.empty(max(S, 1), dtype=torch.int32, device=dev)
+    rows = torch.empty((max(S, 1), H // 2 + H // 16), dtype=torch.uint8, device=dev)
+    expert = torch.empty(max(S, 1), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _workspace(lib().moe_ep_dispatch_workspace_size(T, k, G), dev)
+    _check("moe_ep_dispatch", lib().moe_ep_dispatch(
+        _ptr(topk_ids), T, k, E, G, _ptr(q_tok), _ptr(sf_tok), H, _ptr(counts), _ptr(pos),
+        _ptr(rows), _ptr(expert), _ptr(ws), ws.numel(), _stream(stream)))
+    return counts, pos[:S], rows[:S], expert[:S], ws
+
+
+def ep_scatter(recv_rows: torch.Tensor, H: int, slot_of: torch.Tensor, out_rows: int,
+               xq: torch.Tensor, xsf_mma: torch.Tensor, stream=None):
+    n = recv_rows.shape[0]
+    _check("moe_ep_scatter", lib().moe_ep_scatter(
+        _ptr(recv_rows) if n else None, n, H, _ptr(slot_of) if n else None, out_rows, _ptr(xq),
+        _ptr(xsf_mma), _stream(stream)))
+
+
+def ep_gather(slot_out: torch.Tensor, slot_of: torch.Tensor, n: int, stream=None) -> torch.Tensor:
+    H = slot_out.shape[1]
+    code = {torch.bfloat16: BF16, torch.float32: F32, torch.float16: F16}[slot_out.dtype]
+    out = torch.empty((n, H), dtype=slot_out.dtype, device=slot_out.device)
+    if n:
+        _check("moe_ep_gather", lib().moe_ep_gather(_ptr(slot_out), code, H, _ptr(slot_of), n,
+                                                    _ptr(out), _stream(stream)))
+    return out
 
 
 # ------------------------------------------------------------------ step 7 --

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(CSRC, "_build")
 LIB = os.path.join(PKG, "libnvfp4moe.so")
-SOURCES = ["api.cu", "quantize.cu", "route.cu", "reduce.cu", "gemm.cu", "router.cu", "peak.cu"]
+SOURCES = ["api.cu", "quantize.cu", "route.cu", "reduce.cu", "gemm.cu", "router.cu", "peak.cu",
+           "ep.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",

@@ -275,6 +275,47 @@ int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
                                              stream), 1));
 }
 
+int nvfp4_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, float* amax_out, void* ws,
+               size_t ws_bytes, cudaStream_t stream) {
+  if (rows < 0 || cols <= 0) return NVMOE_ERR_INVALID_ARG;
+  if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (cols % 64 != 0 || !elems_fit(rows, cols)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (amax_out == nullptr || ws == nullptr || (rows > 0 && x == nullptr))
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(ws)) return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < nvfp4_quantize_workspace_size(rows, cols)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  Carve c{static_cast<uint8_t*>(ws)};
+  c.take<int>(kStatusBytes);
+  float* partial = c.take<float>(kQuantMaxPartials * sizeof(float));
+  const int64_t n = rows * cols;
+  int parts = 0;
+  if (n > 0) {
+    parts = quant_amax_blocks(n);
+    const cudaError_t e = counted(launch_quant_amax(x, x_dtype, n, partial, parts, stream), 1);
+    if (e != cudaSuccess) return fail(e);
+  }
+  return status_of(counted(launch_max_reduce(partial, parts, amax_out, stream), 1));
+}
+
+int nvfp4_quantize_act_amax(const void* x, int x_dtype, int64_t rows, int64_t cols,
+                            const int32_t* row_dst, int fanout, int64_t out_rows,
+                            const float* amax_in, uint8_t* q, uint8_t* sf_rowmajor,
+                            uint8_t* sf_mma, float* gs_out, cudaStream_t stream) {
+  if (rows < 0 || cols <= 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
+  if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
+  if (cols % 64 != 0 || !elems_fit(rows, cols) || !elems_fit(out_rows, cols))
+    return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (fanout < 1 || fanout > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  if (row_dst != nullptr && !slots_fit(rows, fanout)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (row_dst == nullptr && (fanout != 1 || out_rows < rows)) return NVMOE_ERR_INVALID_ARG;
+  if (gs_out == nullptr || amax_in == nullptr) return NVMOE_ERR_INVALID_ARG;
+  if (rows > 0 && (x == nullptr || q == nullptr)) return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf_mma)) return NVMOE_ERR_MISALIGNED;
+  return status_of(counted(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr,
+                                             amax_in, 1, q, sf_rowmajor, sf_mma, gs_out,
+                                             stream), 1));
+}
+
 // ----------------------------------------------------------- weights ----
 size_t nvfp4_quantize_weights_workspace_size(int E, int K, int N) {
   (void)K;
@@ -353,7 +394,8 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
                         const float* gs_x, const int32_t* expert_offsets,
                         const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
                         void* slot_out, int slot_out_dtype, const nvmoe_taps* taps, void* ws,
-                        size_t ws_bytes, cudaStream_t stream, LayerLaunch* layer);
+                        size_t ws_bytes, cudaStream_t stream, LayerLaunch* layer,
+                        int phase = 0, float* amax_h = nullptr);
 
 int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
                       const float* gs_x, const int32_t* expert_offsets,
@@ -365,12 +407,28 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
                       slot_out, slot_out_dtype, taps, ws, ws_bytes, stream, nullptr);
 }
 
+int moe_nvfp4_forward_phase(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
+                            const float* gs_x, const int32_t* expert_offsets,
+                            const int32_t* expert_counts, const int32_t* row_token, int64_t T,
+                            int k, void* slot_out, int slot_out_dtype, int phase, float* amax_h,
+                            const nvmoe_taps* taps, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  if (phase != 1 && phase != 2) return NVMOE_ERR_INVALID_ARG;
+  if (taps != nullptr && taps->path == NVMOE_PATH_LAYER) return NVMOE_ERR_INVALID_ARG;
+  return forward_impl(w, xq, xsf_mma, gs_x, expert_offsets, expert_counts, row_token, T, k,
+                      slot_out, slot_out_dtype, taps, ws, ws_bytes, stream, nullptr, phase,
+                      amax_h);
+}
+
 static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* xsf_mma,
                         const float* gs_x, const int32_t* expert_offsets,
                         const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
                         void* slot_out, int slot_out_dtype, const nvmoe_taps* taps, void* ws,
-                        size_t ws_bytes, cudaStream_t stream, LayerLaunch* layer) {
+                        size_t ws_bytes, cudaStream_t stream, LayerLaunch* layer, int phase,
+                        float* amax_h) {
   if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
+  if (phase < 0 || phase > 2 || (phase != 0 && (layer != nullptr || amax_h == nullptr)))
+    return NVMOE_ERR_INVALID_ARG;
   if (slot_out_dtype != NVMOE_BF16 && slot_out_dtype != NVMOE_F32 && slot_out_dtype != NVMOE_F16)
     return NVMOE_ERR_INVALID_ARG;
   // the single-kernel layer path reduces from fp32 slot rows inside the kernel
@@ -394,7 +452,12 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
     return NVMOE_ERR_INVALID_ARG;
   const bool allow_pair = path != NVMOE_PATH_SEPARATE_SINGLE;
   if (path == NVMOE_PATH_SEPARATE_SINGLE) path = NVMOE_PATH_SEPARATE;
-  if (T == 0) return NVMOE_OK;
+  if (phase != 0) path = NVMOE_PATH_SEPARATE;   // the phases are the three-launch path, split
+  if (T == 0) {
+    // an empty batch still reports max |h| = 0 (the caller reduces it over ranks)
+    if (phase == 1) return status_of(counted(launch_max_reduce(nullptr, 0, amax_h, stream), 1));
+    return NVMOE_OK;
+  }
   FwdBuffers b;
   forward_layout(T, k, E, I, static_cast<uint8_t*>(ws), &b);
   float* tap_l1 = nullptr;
@@ -521,13 +584,23 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
     return NVMOE_OK;
   }
   const int g1 = grid_for(tiles1);
-  cudaError_t e = counted(launch_gemm(a1, map_x, map_w1, g1, mt_min * a1.n_tiles, allow_pair, stream), 1);
-  if (e != cudaSuccess) return fail(e);
-  if (timed && note(cudaEventRecord(ev[1], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (phase != 2) {
+    e = counted(launch_gemm(a1, map_x, map_w1, g1, mt_min * a1.n_tiles, allow_pair, stream), 1);
+    if (e != cudaSuccess) return fail(e);
+    if (timed && note(cudaEventRecord(ev[1], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
+  }
+  if (phase == 1) {
+    // max |h| of this call's rows, for the caller to reduce before phase 2
+    return status_of(counted(launch_max_reduce(b.amax, g1, amax_h, stream), 1));
+  }
   if (w->gs_mid == nullptr) {
-    // requantise h over the valid rows (global amax from the L1 partials);
-    // with a static intermediate scale the L1 epilogue has done it
-    e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, b.amax, g1,
+    // requantise h over the valid rows (global amax from the L1 partials, or
+    // in phase 2 the caller's amax); with a static intermediate scale the L1
+    // epilogue has done it
+    const float* amax_src = phase == 2 ? amax_h : b.amax;
+    const int n_amax = phase == 2 ? 1 : g1;
+    e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, amax_src, n_amax,
                                   b.hq, nullptr, b.hsf, b.gs_h, stream), 1);
     if (e != cudaSuccess) return fail(e);
   }
@@ -537,6 +610,95 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   if (e != cudaSuccess) return fail(e);
   if (timed && note(cudaEventRecord(ev[3], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
   return NVMOE_OK;
+}
+
+// --------------------------------------------------- expert parallel ----
+namespace {
+struct EpBuffers {
+  uint8_t* route_ws;
+  size_t route_ws_bytes;
+  int32_t* dest;
+  int32_t* padded;
+  int32_t* offsets;
+  int32_t* row_token;
+};
+
+size_t ep_layout(int64_t T, int k, int G, uint8_t* base, EpBuffers* b) {
+  const int64_t S = T * k;
+  Carve c{base};
+  b->route_ws_bytes = moe_route_workspace_size(T, k, G);
+  b->route_ws = c.take<uint8_t>(b->route_ws_bytes);          // its status word comes first
+  b->dest = c.take<int32_t>(static_cast<size_t>(S > 0 ? S : 1) * sizeof(int32_t));
+  b->padded = c.take<int32_t>(static_cast<size_t>(S > 0 ? S : 1) * sizeof(int32_t));
+  b->offsets = c.take<int32_t>(static_cast<size_t>(G + 1) * sizeof(int32_t));
+  const int64_t rows = rows_bound(T, k, G);
+  b->row_token = c.take<int32_t>(static_cast<size_t>(rows > 0 ? rows : 1) * sizeof(int32_t));
+  return c.off;
+}
+}  // namespace
+
+size_t moe_ep_dispatch_workspace_size(int64_t T, int k, int G) {
+  if (T < 0 || k < 1 || G < 1 || G > kMaxExperts || !slots_fit(T, k)) return 0;
+  EpBuffers b;
+  return ep_layout(T, k, G, nullptr, &b);
+}
+
+int moe_ep_dispatch(const int32_t* topk_ids, int64_t T, int k, int E, int G, const uint8_t* q_tok,
+                    const uint8_t* sf_tok, int H, int32_t* send_counts, int32_t* send_pos,
+                    uint8_t* send_rows, int32_t* send_expert, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts || G < 1 || G > E || E % G != 0)
+    return NVMOE_ERR_INVALID_ARG;
+  if (H < 1 || H % 256 != 0 || !slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (send_counts == nullptr || ws == nullptr) return NVMOE_ERR_INVALID_ARG;
+  if (T > 0 && (topk_ids == nullptr || q_tok == nullptr || sf_tok == nullptr ||
+                send_pos == nullptr || send_rows == nullptr || send_expert == nullptr))
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(q_tok) || !aligned16(sf_tok) || !aligned16(send_rows) || !aligned16(ws))
+    return NVMOE_ERR_MISALIGNED;
+  if (ws_bytes < moe_ep_dispatch_workspace_size(T, k, G)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
+  EpBuffers b;
+  ep_layout(T, k, G, static_cast<uint8_t*>(ws), &b);
+  const int64_t S = T * k;
+  int* status = reinterpret_cast<int*>(b.route_ws);
+  if (S > 0) {
+    const cudaError_t e = counted(launch_ep_dest(topk_ids, S, E, G, b.dest, status, stream), 1);
+    if (e != cudaSuccess) return fail(e);
+  }
+  // counting sort of the slots by destination (stable in t*k + j), the
+  // routing kernels with ranks for experts; send_counts = the true counts
+  const int st = moe_route_permute(b.dest, T, k, G, b.offsets, send_counts, b.row_token, b.padded,
+                                   b.route_ws, b.route_ws_bytes, stream);
+  if (st != NVMOE_OK || S == 0) return st;
+  return status_of(counted(launch_ep_pack(topk_ids, b.padded, b.dest, b.offsets, send_counts, S, k,
+                                          E, G, q_tok, sf_tok, H, send_pos, send_rows,
+                                          send_expert, stream), 1));
+}
+
+int moe_ep_scatter(const uint8_t* recv_rows, int64_t n, int H, const int32_t* slot_of,
+                   int64_t out_rows, uint8_t* xq, uint8_t* xsf_mma, cudaStream_t stream) {
+  if (n < 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
+  if (H < 1 || H % 256 != 0 || !elems_fit(out_rows, H)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return NVMOE_OK;
+  if (recv_rows == nullptr || slot_of == nullptr || xq == nullptr || xsf_mma == nullptr)
+    return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(recv_rows) || !aligned16(xq) || !aligned16(xsf_mma)) return NVMOE_ERR_MISALIGNED;
+  const int k_atoms = static_cast<int>(round_up(H, kStageK) / 64);
+  return status_of(counted(launch_ep_scatter(recv_rows, n, H, slot_of, xq, xsf_mma, k_atoms,
+                                             stream), 1));
+}
+
+int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, const int32_t* slot_of,
+                  int64_t n, void* out_rows, cudaStream_t stream) {
+  if (n < 0 || H < 1) return NVMOE_ERR_INVALID_ARG;
+  if (slot_out_dtype != NVMOE_BF16 && slot_out_dtype != NVMOE_F32 && slot_out_dtype != NVMOE_F16)
+    return NVMOE_ERR_INVALID_ARG;
+  const int64_t row_bytes = static_cast<int64_t>(H) * (slot_out_dtype == NVMOE_F32 ? 4 : 2);
+  if (row_bytes % 16 != 0) return NVMOE_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return NVMOE_OK;
+  if (slot_out == nullptr || slot_of == nullptr || out_rows == nullptr) return NVMOE_ERR_INVALID_ARG;
+  if (!aligned16(slot_out) || !aligned16(out_rows)) return NVMOE_ERR_MISALIGNED;
+  return status_of(counted(launch_ep_gather(slot_out, row_bytes, slot_of, n, out_rows, stream), 1));
 }
 
 // ------------------------------------------------------------ router ----

@@ -67,6 +67,20 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
                               uint8_t* sf_row, uint8_t* sf_mma, float* gs_out,
                               cudaStream_t stream);
 int quant_amax_blocks(int64_t n_elems);
+
+// ---- expert-parallel dispatch / combine (ep.cu) ----
+cudaError_t launch_ep_dest(const int32_t* ids, int64_t S, int E, int G, int32_t* dest, int* status,
+                           cudaStream_t stream);
+cudaError_t launch_ep_pack(const int32_t* ids, const int32_t* padded, const int32_t* dest,
+                           const int32_t* offsets, const int32_t* counts, int64_t S, int k, int E,
+                           int G, const uint8_t* q_tok, const uint8_t* sf_tok, int H,
+                           int32_t* send_pos, uint8_t* send_rows, int32_t* send_expert,
+                           cudaStream_t stream);
+cudaError_t launch_ep_scatter(const uint8_t* rows, int64_t n, int H, const int32_t* slot_of,
+                              uint8_t* xq, uint8_t* xsf, int k_atoms, cudaStream_t stream);
+cudaError_t launch_ep_gather(const void* slot_out, int64_t row_bytes, const int32_t* slot_of,
+                             int64_t n, void* out, cudaStream_t stream);
+cudaError_t launch_max_reduce(const float* partial, int n, float* out, cudaStream_t stream);
 // Both passes in one CTA, for inputs of at most kQuantSmallElems elements.
 constexpr int64_t kQuantSmallElems = 64 * 1024;
 cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t cols,
