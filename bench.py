@@ -16,8 +16,11 @@ idle, Student-t activations), the largest of the workloads, whose roofline is
 the dense FP4 tensor peak.  --config decode1 (one token) and the others
 select the smaller workloads; decode workloads are bound by HBM bandwidth on
 the weight + scale bytes of the experts that receive a token.  The L2 cache
-is flushed (256 MiB write) before every timed step; inputs are resident in
-HBM before the timed region.
+is flushed (256 MiB write) before every timed step of the large workloads;
+decode steps instead alternate two routings with disjoint expert sets (each
+step's weights are larger than L2 and were not read by the step before), and
+the flushed decode time is reported in config.  Inputs are resident in HBM
+before the timed region.
 
 Also reported:
   roofline      the dominant kernel (the single layer kernel for small batches,
@@ -521,28 +524,53 @@ def main():
         layer.forward(x, ids, w)
     stream.synchronize()
     assert layer.status() == 0
+    # Small batches (decode): consecutive steps alternate two routings whose
+    # expert sets are disjoint (expert ids shifted by E/2) instead of flushing
+    # L2: a step's weights (its experts', >= 8 x 37 MB) are larger than the
+    # L2 and none were read by the step before, while the kernel's code
+    # stays cached as it would across the layers of a model.  The flushed
+    # timing is reported beside it.  Large batches flush L2 before each step.
+    rotate = cfg.T * cfg.k <= 2048
+    steps_fns = [graph.replay]
+    ids_alt = [ids]
+    if rotate:
+        ids_b = ((ids.long() + cfg.E // 2) % cfg.E).to(torch.int32)
+        graph_b = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            layer.forward(x, ids_b, w)
+        stream.synchronize()
+        with torch.cuda.graph(graph_b, stream=stream):
+            layer.forward(x, ids_b, w)
+        stream.synchronize()
+        steps_fns.append(graph_b.replay)
+        ids_alt.append(ids_b)
 
-    def timed_loop(n, step_fn):
+    def timed_loop(n, step_fn, flush_l2=True):
+        fns = step_fn if isinstance(step_fn, list) else [step_fn]
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         with torch.cuda.stream(stream):
             for i in range(n):
-                flush.fill_(i & 0xFF)
+                if flush_l2:
+                    flush.fill_(i & 0xFF)
                 starts[i].record(stream)
-                step_fn()
+                fns[i % len(fns)]()
                 ends[i].record(stream)
         stream.synchronize()
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
-    timed_loop(args.warmup, graph.replay)
+    timed_loop(args.warmup, steps_fns, flush_l2=not rotate)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    times = timed_loop(args.steps, graph.replay)
+    times = timed_loop(args.steps, steps_fns, flush_l2=not rotate)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    flushed_ms = None
+    if rotate:
+        flushed_ms = sum(timed_loop(args.steps, graph.replay)) / args.steps
     if world > 1:
         torch.distributed.barrier()
     total_ms = max_over_ranks(sum(times), world, dev)
@@ -555,8 +583,9 @@ def main():
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     with torch.cuda.stream(stream):
         for i in range(n_prof):
-            flush.fill_(i & 0xFF)
-            layer.forward(x, ids, w, taps={"stage_events": evs})
+            if not rotate:
+                flush.fill_(i & 0xFF)
+            layer.forward(x, ids_alt[i % len(ids_alt)], w, taps={"stage_events": evs})
             stream.synchronize()
             stage["l1"].append(evs[0].elapsed_time(evs[1]))
             stage["requant"].append(evs[1].elapsed_time(evs[2]))
@@ -693,7 +722,11 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "nvfp4 (e2m1 x e4m3 scales), fp32 accumulate", "data": "synthetic",
-            "config": {"workload": workload_desc(cfg), "l2_flush": "256 MiB write before every step",
+            "config": {"workload": workload_desc(cfg),
+                       "l2_flush": ("none: consecutive steps use disjoint expert sets, whose "
+                                    "weights are larger than L2 (ms_per_step with a 256 MiB "
+                                    "flush before every step: %.4f)" % flushed_ms) if rotate
+                                   else "256 MiB write before every step",
                        "graph": "one CUDA graph per step", "active_experts": E_act,
                        "api": "moe_nvfp4_layer_forward" if args.api == "layer"
                               else "route + quantise + forward + reduce",

@@ -71,8 +71,11 @@ typedef enum {
   NVMOE_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed     */
   NVMOE_ERR_TIMEOUT = 6,            /* device: a bounded wait ran out        */
   NVMOE_ERR_DEVICE_BAD_INDEX = 7,   /* device: expert id out of [0, E)       */
-  NVMOE_ERR_RANGE = 8               /* device: a value exceeded the range of
+  NVMOE_ERR_RANGE = 8,              /* device: a value exceeded the range of
                                        its storage type (fp16 slot rows)     */
+  NVMOE_ERR_DEVICE_BOUNDS = 9       /* device, NVMOE_DEBUG_BOUNDS build only:
+                                       an index outside its buffer; the
+                                       access was skipped                    */
 } nvmoe_status;
 
 /* Element types of activation / output buffers. */
@@ -441,7 +444,9 @@ int nvfp4_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, float* am
 /* nvfp4_quantize_act with the amax given (*amax_in, device float) instead of
  * computed: gs = amax/2688 written to *gs_out; no workspace.  The same
  * arguments and results as nvfp4_quantize_act otherwise (its results equal
- * nvfp4_quantize_act's when *amax_in is the matrix's own amax). */
+ * nvfp4_quantize_act's when *amax_in is the matrix's own amax).  Having no
+ * status word, the NVMOE_DEBUG_BOUNDS build skips a row_dst >= out_rows
+ * without a record. */
 int nvfp4_quantize_act_amax(const void* x, int x_dtype, int64_t rows, int64_t cols,
                             const int32_t* row_dst, int fanout, int64_t out_rows,
                             const float* amax_in, uint8_t* q, uint8_t* sf_rowmajor,
@@ -469,18 +474,25 @@ int moe_ep_dispatch(const int32_t* topk_ids, int64_t T, int k, int E, int G,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Received rows (moe_ep_dispatch's row format, n of them) into the slot
- * layout of moe_nvfp4_forward: row i's nibbles to xq[slot_of[i]] and its
- * scales to their staged offsets in xsf_mma (nvfp4_sf_mma_bytes(out_rows, H));
- * slot_of from moe_route_permute of the received expert ids (k = 1); rows
- * with slot_of < 0 are skipped.  16-byte alignment of recv_rows, xq, xsf_mma. */
+ * layout of moe_nvfp4_forward: row i's nibbles to xq[slot_of[i]] (xq has
+ * out_rows rows) and its scales to their staged offsets in xsf_mma
+ * (nvfp4_sf_mma_bytes(out_rows, H)); slot_of from moe_route_permute of the
+ * received expert ids (k = 1); rows with slot_of < 0 are skipped.  status:
+ * nullable device int where the NVMOE_DEBUG_BOUNDS build records
+ * NVMOE_ERR_DEVICE_BOUNDS for a slot_of >= out_rows (that row is skipped).
+ * 16-byte alignment of recv_rows, xq, xsf_mma. */
 int moe_ep_scatter(const uint8_t* recv_rows, int64_t n, int H, const int32_t* slot_of,
-                   int64_t out_rows, uint8_t* xq, uint8_t* xsf_mma, cudaStream_t stream);
+                   int64_t out_rows, uint8_t* xq, uint8_t* xsf_mma, int* status,
+                   cudaStream_t stream);
 
-/* out_rows[i] = slot_out[slot_of[i]] for i < n (H elements of slot_out_dtype
- * per row; a row with slot_of < 0 is zero): the owner's slot outputs in
- * received order, for the return exchange.  16-byte alignment. */
-int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, const int32_t* slot_of,
-                  int64_t n, void* out_rows, cudaStream_t stream);
+/* out_rows[i] = slot_out[slot_of[i]] for i < n (slot_out: slot_rows rows of
+ * H elements of slot_out_dtype; a row with slot_of < 0 is zero): the owner's
+ * slot outputs in received order, for the return exchange.  status as for
+ * moe_ep_scatter (a slot_of >= slot_rows gives a zero row in that build).
+ * 16-byte alignment. */
+int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, int64_t slot_rows,
+                  const int32_t* slot_of, int64_t n, void* out_rows, int* status,
+                  cudaStream_t stream);
 
 /* -------------------------------------------------------- router front end --
  * moe_router_topk — the step before the routing permutation.  The pages keep

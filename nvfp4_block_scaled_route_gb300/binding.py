@@ -15,7 +15,10 @@ from typing import Optional
 import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libnvfp4moe.so")
+# NVMOE_LIBRARY=debug loads the debug-bounds build (in-kernel index checks
+# that record NVMOE_ERR_DEVICE_BOUNDS instead of touching memory out of range)
+LIB_PATH = os.path.join(PKG, "libnvfp4moe_debug.so" if os.environ.get("NVMOE_LIBRARY") == "debug"
+                        else "libnvfp4moe.so")
 
 BF16, F32, F16 = 0, 1, 2
 NVMOE_ERR_CUDA = 5
@@ -84,8 +87,8 @@ SIGNATURES = {
     "nvfp4_quantize_act_amax": (_I, [_P, _I, _I64, _I64, _P, _I, _I64, _P, _P, _P, _P, _P, _P]),
     "moe_ep_dispatch_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_ep_dispatch": (_I, [_P, _I64, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_ep_scatter": (_I, [_P, _I64, _I, _P, _I64, _P, _P, _P]),
-    "moe_ep_gather": (_I, [_P, _I, _I, _P, _I64, _P, _P]),
+    "moe_ep_scatter": (_I, [_P, _I64, _I, _P, _I64, _P, _P, _P, _P]),
+    "moe_ep_gather": (_I, [_P, _I, _I, _I64, _P, _I64, _P, _P, _P]),
     "moe_nvfp4_layer_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_nvfp4_layer_forward": (_I, [ctypes.POINTER(Weights), _P, _I, _P, _P, _I64, _I, _P, _I,
                                      ctypes.POINTER(Taps), _P, _SZ, _P]),
@@ -452,20 +455,24 @@ def ep_dispatch(topk_ids: torch.Tensor, E: int, G: int, q_tok: torch.Tensor,
 
 
 def ep_scatter(recv_rows: torch.Tensor, H: int, slot_of: torch.Tensor, out_rows: int,
-               xq: torch.Tensor, xsf_mma: torch.Tensor, stream=None):
+               xq: torch.Tensor, xsf_mma: torch.Tensor, status: Optional[torch.Tensor] = None,
+               stream=None):
+    """status: optional int32 [1] device tensor (debug-bounds records)."""
     n = recv_rows.shape[0]
     _check("moe_ep_scatter", lib().moe_ep_scatter(
         _ptr(recv_rows) if n else None, n, H, _ptr(slot_of) if n else None, out_rows, _ptr(xq),
-        _ptr(xsf_mma), _stream(stream)))
+        _ptr(xsf_mma), _ptr(status), _stream(stream)))
 
 
-def ep_gather(slot_out: torch.Tensor, slot_of: torch.Tensor, n: int, stream=None) -> torch.Tensor:
+def ep_gather(slot_out: torch.Tensor, slot_of: torch.Tensor, n: int,
+              status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     H = slot_out.shape[1]
     code = {torch.bfloat16: BF16, torch.float32: F32, torch.float16: F16}[slot_out.dtype]
     out = torch.empty((n, H), dtype=slot_out.dtype, device=slot_out.device)
     if n:
-        _check("moe_ep_gather", lib().moe_ep_gather(_ptr(slot_out), code, H, _ptr(slot_of), n,
-                                                    _ptr(out), _stream(stream)))
+        _check("moe_ep_gather", lib().moe_ep_gather(_ptr(slot_out), code, H, slot_out.shape[0],
+                                                    _ptr(slot_of), n, _ptr(out), _ptr(status),
+                                                    _stream(stream)))
     return out
 
 

@@ -1,6 +1,7 @@
 // C-ABI entry points of libnvfp4moe.so (declared in include/nvfp4moe.h):
 // argument checks, workspace carving, TMA descriptor encoding and kernel
 // launches.  No allocation, no host synchronisation on the compute calls.
+#include <nvtx3/nvToolsExt.h>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -68,6 +69,15 @@ bool make_tiled_map(CUtensorMap* map, const void* base, int64_t n_tiles) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+// NVTX range around each call that enqueues GPU work: named for the entry
+// point in a tool's timeline (nsys, ncu --nvtx); a few ns without a tool.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -152,6 +162,7 @@ const char* nvmoe_status_str(int s) {
     case NVMOE_ERR_TIMEOUT: return "device wait timed out";
     case NVMOE_ERR_DEVICE_BAD_INDEX: return "expert id out of range";
     case NVMOE_ERR_RANGE: return "value beyond the range of its storage type";
+    case NVMOE_ERR_DEVICE_BOUNDS: return "index outside its buffer (debug-bounds build)";
     default: return "unknown status";
   }
 }
@@ -183,6 +194,7 @@ size_t nvfp4_sf_mma_bytes(int64_t rows, int64_t cols) {
 // ------------------------------------------------------- FP4 probe ----
 int nvmoe_fp4_mma_probe(int variant, int iters, int grid, long long* cycles, void* ws,
                         size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("nvmoe_fp4_mma_probe");
   if (variant < 0 || variant > 2047 || ((variant & kProbeCp32) && (variant & kProbeCp256)))
     return NVMOE_ERR_INVALID_ARG;
   // four accumulators of 128 columns fill the 512 TMEM columns: N = 128 only
@@ -220,6 +232,7 @@ size_t moe_route_workspace_size(int64_t T, int k, int E) {
 int moe_route_permute(const int32_t* topk_ids, int64_t T, int k, int E, int32_t* expert_offsets,
                       int32_t* expert_counts, int32_t* row_token, int32_t* slot_of, void* ws,
                       size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_route_permute");
   if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts) return NVMOE_ERR_INVALID_ARG;
   if (!slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (expert_offsets == nullptr || expert_counts == nullptr || ws == nullptr)
@@ -248,6 +261,7 @@ int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
                        const int32_t* row_dst, int fanout, int64_t out_rows, uint8_t* q,
                        uint8_t* sf_rowmajor, uint8_t* sf_mma, float* gs_out, void* ws,
                        size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("nvfp4_quantize_act");
   if (rows < 0 || cols <= 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
   if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
   if (cols % 64 != 0 || !elems_fit(rows, cols) || !elems_fit(out_rows, cols))
@@ -261,22 +275,24 @@ int nvfp4_quantize_act(const void* x, int x_dtype, int64_t rows, int64_t cols,
     return NVMOE_ERR_MISALIGNED;
   if (ws_bytes < nvfp4_quantize_workspace_size(rows, cols)) return NVMOE_ERR_WORKSPACE_TOO_SMALL;
   Carve c{static_cast<uint8_t*>(ws)};
-  c.take<int>(kStatusBytes);
+  int* status = c.take<int>(kStatusBytes);
   float* partial = c.take<float>(kQuantMaxPartials * sizeof(float));
   const int64_t n = rows * cols;
   if (n <= kQuantSmallElems)
     return status_of(counted(launch_quant_small(x, x_dtype, rows, cols, row_dst, fanout, q,
-                                                sf_rowmajor, sf_mma, gs_out, stream), 1));
+                                                sf_rowmajor, sf_mma, gs_out, out_rows, status,
+                                                stream), 1));
   const int parts = quant_amax_blocks(n);
   cudaError_t e = counted(launch_quant_amax(x, x_dtype, n, partial, parts, stream), 1);
   if (e != cudaSuccess) return fail(e);
   return status_of(counted(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr,
                                              partial, parts, q, sf_rowmajor, sf_mma, gs_out,
-                                             stream), 1));
+                                             out_rows, status, stream), 1));
 }
 
 int nvfp4_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, float* amax_out, void* ws,
                size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("nvfp4_amax");
   if (rows < 0 || cols <= 0) return NVMOE_ERR_INVALID_ARG;
   if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
   if (cols % 64 != 0 || !elems_fit(rows, cols)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
@@ -301,6 +317,7 @@ int nvfp4_quantize_act_amax(const void* x, int x_dtype, int64_t rows, int64_t co
                             const int32_t* row_dst, int fanout, int64_t out_rows,
                             const float* amax_in, uint8_t* q, uint8_t* sf_rowmajor,
                             uint8_t* sf_mma, float* gs_out, cudaStream_t stream) {
+  const NvtxRange nvtx_range("nvfp4_quantize_act_amax");
   if (rows < 0 || cols <= 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
   if (x_dtype != NVMOE_BF16 && x_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
   if (cols % 64 != 0 || !elems_fit(rows, cols) || !elems_fit(out_rows, cols))
@@ -312,8 +329,8 @@ int nvfp4_quantize_act_amax(const void* x, int x_dtype, int64_t rows, int64_t co
   if (rows > 0 && (x == nullptr || q == nullptr)) return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sf_mma)) return NVMOE_ERR_MISALIGNED;
   return status_of(counted(launch_quant_pack(x, x_dtype, rows, cols, row_dst, fanout, nullptr,
-                                             amax_in, 1, q, sf_rowmajor, sf_mma, gs_out,
-                                             stream), 1));
+                                             amax_in, 1, q, sf_rowmajor, sf_mma, gs_out, out_rows,
+                                             nullptr, stream), 1));
 }
 
 // ----------------------------------------------------------- weights ----
@@ -326,6 +343,7 @@ size_t nvfp4_quantize_weights_workspace_size(int E, int K, int N) {
 
 int nvfp4_quantize_weights(const float* w, int E, int K, int N, uint8_t* q, uint8_t* sf,
                            float* gs, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("nvfp4_quantize_weights");
   if (E < 1 || K < 1 || N < 1 || w == nullptr || q == nullptr || sf == nullptr ||
       gs == nullptr || ws == nullptr)
     return NVMOE_ERR_INVALID_ARG;
@@ -348,6 +366,7 @@ size_t moe_nvfp4_prepared_bytes(int E, int K, int N) {
 
 int moe_nvfp4_prepare_weights(const uint8_t* q_ckpt, const uint8_t* sf_ckpt, int E, int K, int N,
                               uint8_t* q_out, uint8_t* sf_out, cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_nvfp4_prepare_weights");
   if (E < 1 || K < 1 || N < 1 || q_ckpt == nullptr || sf_ckpt == nullptr ||
       q_out == nullptr || sf_out == nullptr)
     return NVMOE_ERR_INVALID_ARG;
@@ -402,6 +421,7 @@ int moe_nvfp4_forward(const nvmoe_weights* w, const uint8_t* xq, const uint8_t* 
                       const int32_t* expert_counts, const int32_t* row_token, int64_t T, int k,
                       void* slot_out, int slot_out_dtype, const nvmoe_taps* taps, void* ws,
                       size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_nvfp4_forward");
   if (taps != nullptr && taps->path == NVMOE_PATH_LAYER) return NVMOE_ERR_INVALID_ARG;
   return forward_impl(w, xq, xsf_mma, gs_x, expert_offsets, expert_counts, row_token, T, k,
                       slot_out, slot_out_dtype, taps, ws, ws_bytes, stream, nullptr);
@@ -413,6 +433,7 @@ int moe_nvfp4_forward_phase(const nvmoe_weights* w, const uint8_t* xq, const uin
                             int k, void* slot_out, int slot_out_dtype, int phase, float* amax_h,
                             const nvmoe_taps* taps, void* ws, size_t ws_bytes,
                             cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_nvfp4_forward_phase");
   if (phase != 1 && phase != 2) return NVMOE_ERR_INVALID_ARG;
   if (taps != nullptr && taps->path == NVMOE_PATH_LAYER) return NVMOE_ERR_INVALID_ARG;
   return forward_impl(w, xq, xsf_mma, gs_x, expert_offsets, expert_counts, row_token, T, k,
@@ -514,6 +535,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a1.partials = b.pieces;
   a1.counters = b.counters;
   a1.status = b.status;
+  a1.rows = rows;
   if (taps != nullptr && taps->ready_flag != nullptr) {
     a1.ready_flag = taps->ready_flag;
     a1.ready_value = taps->ready_value;
@@ -542,6 +564,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
   a2.partials = b.pieces;
   a2.counters = b.counters + kMaxSplitTiles;
   a2.status = b.status;
+  a2.rows = rows;
 
   // Tiles that can exist, from the host-side bound on expert segments.
   const int64_t S = T * k;
@@ -601,7 +624,7 @@ static int forward_impl(const nvmoe_weights* w, const uint8_t* xq, const uint8_t
     const float* amax_src = phase == 2 ? amax_h : b.amax;
     const int n_amax = phase == 2 ? 1 : g1;
     e = counted(launch_quant_pack(b.h, NVMOE_F32, rows, I, nullptr, 1, row_token, amax_src, n_amax,
-                                  b.hq, nullptr, b.hsf, b.gs_h, stream), 1);
+                                  b.hq, nullptr, b.hsf, b.gs_h, rows, b.status, stream), 1);
     if (e != cudaSuccess) return fail(e);
   }
   if (timed && note(cudaEventRecord(ev[2], stream)) != cudaSuccess) return NVMOE_ERR_CUDA;
@@ -647,6 +670,7 @@ int moe_ep_dispatch(const int32_t* topk_ids, int64_t T, int k, int E, int G, con
                     const uint8_t* sf_tok, int H, int32_t* send_counts, int32_t* send_pos,
                     uint8_t* send_rows, int32_t* send_expert, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_ep_dispatch");
   if (T < 0 || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts || G < 1 || G > E || E % G != 0)
     return NVMOE_ERR_INVALID_ARG;
   if (H < 1 || H % 256 != 0 || !slots_fit(T, k)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
@@ -676,7 +700,9 @@ int moe_ep_dispatch(const int32_t* topk_ids, int64_t T, int k, int E, int G, con
 }
 
 int moe_ep_scatter(const uint8_t* recv_rows, int64_t n, int H, const int32_t* slot_of,
-                   int64_t out_rows, uint8_t* xq, uint8_t* xsf_mma, cudaStream_t stream) {
+                   int64_t out_rows, uint8_t* xq, uint8_t* xsf_mma, int* status,
+                   cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_ep_scatter");
   if (n < 0 || out_rows < 0) return NVMOE_ERR_INVALID_ARG;
   if (H < 1 || H % 256 != 0 || !elems_fit(out_rows, H)) return NVMOE_ERR_UNSUPPORTED_SHAPE;
   if (n == 0) return NVMOE_OK;
@@ -684,13 +710,15 @@ int moe_ep_scatter(const uint8_t* recv_rows, int64_t n, int H, const int32_t* sl
     return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(recv_rows) || !aligned16(xq) || !aligned16(xsf_mma)) return NVMOE_ERR_MISALIGNED;
   const int k_atoms = static_cast<int>(round_up(H, kStageK) / 64);
-  return status_of(counted(launch_ep_scatter(recv_rows, n, H, slot_of, xq, xsf_mma, k_atoms,
-                                             stream), 1));
+  return status_of(counted(launch_ep_scatter(recv_rows, n, H, slot_of, out_rows, xq, xsf_mma,
+                                             k_atoms, status, stream), 1));
 }
 
-int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, const int32_t* slot_of,
-                  int64_t n, void* out_rows, cudaStream_t stream) {
-  if (n < 0 || H < 1) return NVMOE_ERR_INVALID_ARG;
+int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, int64_t slot_rows,
+                  const int32_t* slot_of, int64_t n, void* out_rows, int* status,
+                  cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_ep_gather");
+  if (n < 0 || H < 1 || slot_rows < 0) return NVMOE_ERR_INVALID_ARG;
   if (slot_out_dtype != NVMOE_BF16 && slot_out_dtype != NVMOE_F32 && slot_out_dtype != NVMOE_F16)
     return NVMOE_ERR_INVALID_ARG;
   const int64_t row_bytes = static_cast<int64_t>(H) * (slot_out_dtype == NVMOE_F32 ? 4 : 2);
@@ -698,7 +726,8 @@ int moe_ep_gather(const void* slot_out, int slot_out_dtype, int H, const int32_t
   if (n == 0) return NVMOE_OK;
   if (slot_out == nullptr || slot_of == nullptr || out_rows == nullptr) return NVMOE_ERR_INVALID_ARG;
   if (!aligned16(slot_out) || !aligned16(out_rows)) return NVMOE_ERR_MISALIGNED;
-  return status_of(counted(launch_ep_gather(slot_out, row_bytes, slot_of, n, out_rows, stream), 1));
+  return status_of(counted(launch_ep_gather(slot_out, row_bytes, slot_rows, slot_of, n, out_rows,
+                                            status, stream), 1));
 }
 
 // ------------------------------------------------------------ router ----
@@ -710,6 +739,7 @@ size_t moe_router_workspace_size(int64_t T, int H, int E) {
 int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E, int k,
                     int softmax_mode, int32_t* topk_ids, float* topk_w, void* ws,
                     size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_router_topk");
   if (T < 0 || H < 1 || E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopK || k > E)
     return NVMOE_ERR_INVALID_ARG;
   if (softmax_mode != NVMOE_ROUTER_SELECTED && softmax_mode != NVMOE_ROUTER_ALL)
@@ -740,6 +770,7 @@ int moe_router_topk(const void* x, const void* w_router, int64_t T, int H, int E
 int moe_unpermute_reduce(const void* slot_out, int slot_out_dtype, const int32_t* slot_of,
                          const float* topk_w, int64_t T, int k, int64_t H, void* y, int y_dtype,
                          cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_unpermute_reduce");
   if (T < 0 || k < 1 || k > kMaxTopK || H < 1) return NVMOE_ERR_INVALID_ARG;
   if (y_dtype != NVMOE_BF16 && y_dtype != NVMOE_F32) return NVMOE_ERR_INVALID_ARG;
   if (slot_out_dtype != NVMOE_BF16 && slot_out_dtype != NVMOE_F32 && slot_out_dtype != NVMOE_F16)
@@ -806,6 +837,7 @@ int moe_nvfp4_layer_forward(const nvmoe_weights* w, const void* x, int x_dtype,
                             const int32_t* topk_ids, const float* topk_w, int64_t T, int k,
                             void* y, int y_dtype, const nvmoe_taps* taps, void* ws,
                             size_t ws_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("moe_nvfp4_layer_forward");
   if (w == nullptr || T < 0 || k < 1 || k > kMaxTopK) return NVMOE_ERR_INVALID_ARG;
   const int E = w->E, H = w->H, I = w->I;
   if (E < 1 || E > kMaxExperts || H < 1 || I < 1) return NVMOE_ERR_INVALID_ARG;

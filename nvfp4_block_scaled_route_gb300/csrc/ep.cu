@@ -95,8 +95,9 @@ __global__ void ep_pack_kernel(const int32_t* __restrict__ ids, const int32_t* _
 // One warp per received row: nibbles to xq[slot_of[i]], the H/16 scale
 // bytes to their staged offsets (4 consecutive groups form one 32-bit word).
 __global__ void ep_scatter_kernel(const uint8_t* __restrict__ rows, int64_t n, int H,
-                                  const int32_t* __restrict__ slot_of, uint8_t* __restrict__ xq,
-                                  uint8_t* __restrict__ xsf, int k_atoms) {
+                                  const int32_t* __restrict__ slot_of, int64_t out_rows,
+                                  uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf,
+                                  int k_atoms, int* status) {
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int qb = H / 2, sb = H / 16;
@@ -104,7 +105,7 @@ __global__ void ep_scatter_kernel(const uint8_t* __restrict__ rows, int64_t n, i
   for (int64_t i = blockIdx.x * (int64_t)warps + (threadIdx.x >> 5); i < n;
        i += (int64_t)gridDim.x * warps) {
     const int64_t r = slot_of[i];
-    if (r < 0) continue;
+    if (r < 0 || !NVMOE_BOUNDS(r < out_rows, status)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(rows + i * row_bytes);
     uint4* dst = reinterpret_cast<uint4*>(xq + r * qb);
     for (int c = lane; c < qb / 16; c += 32) dst[c] = src[c];
@@ -116,15 +117,15 @@ __global__ void ep_scatter_kernel(const uint8_t* __restrict__ rows, int64_t n, i
 
 // out[i] = slot_out[slot_of[i]] (row_bytes per row, a multiple of 16).
 __global__ void ep_gather_kernel(const uint8_t* __restrict__ slot_out, int64_t row_bytes,
-                                 const int32_t* __restrict__ slot_of, int64_t n,
-                                 uint8_t* __restrict__ out) {
+                                 int64_t slot_rows, const int32_t* __restrict__ slot_of, int64_t n,
+                                 uint8_t* __restrict__ out, int* status) {
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   for (int64_t i = blockIdx.x * (int64_t)warps + (threadIdx.x >> 5); i < n;
        i += (int64_t)gridDim.x * warps) {
     const int64_t r = slot_of[i];
     uint4* dst = reinterpret_cast<uint4*>(out + i * row_bytes);
-    if (r < 0) {
+    if (r < 0 || !NVMOE_BOUNDS(r < slot_rows, status)) {
       for (int c = lane; c < row_bytes / 16; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
       continue;
     }
@@ -179,16 +180,19 @@ cudaError_t launch_ep_pack(const int32_t* ids, const int32_t* padded, const int3
 }
 
 cudaError_t launch_ep_scatter(const uint8_t* rows, int64_t n, int H, const int32_t* slot_of,
-                              uint8_t* xq, uint8_t* xsf, int k_atoms, cudaStream_t stream) {
-  ep_scatter_kernel<<<ep_blocks(n), kEpThreads, 0, stream>>>(rows, n, H, slot_of, xq, xsf,
-                                                            k_atoms);
+                              int64_t out_rows, uint8_t* xq, uint8_t* xsf, int k_atoms,
+                              int* status, cudaStream_t stream) {
+  ep_scatter_kernel<<<ep_blocks(n), kEpThreads, 0, stream>>>(rows, n, H, slot_of, out_rows, xq,
+                                                            xsf, k_atoms, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_ep_gather(const void* slot_out, int64_t row_bytes, const int32_t* slot_of,
-                             int64_t n, void* out, cudaStream_t stream) {
+cudaError_t launch_ep_gather(const void* slot_out, int64_t row_bytes, int64_t slot_rows,
+                             const int32_t* slot_of, int64_t n, void* out, int* status,
+                             cudaStream_t stream) {
   ep_gather_kernel<<<ep_blocks(n), kEpThreads, 0, stream>>>(
-      static_cast<const uint8_t*>(slot_out), row_bytes, slot_of, n, static_cast<uint8_t*>(out));
+      static_cast<const uint8_t*>(slot_out), row_bytes, slot_rows, slot_of, n,
+      static_cast<uint8_t*>(out), status);
   return cudaGetLastError();
 }
 

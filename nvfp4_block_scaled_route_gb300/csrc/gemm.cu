@@ -122,6 +122,13 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
   return ti;
 }
 
+// The valid rows of a tile (rows row0 + [0, n_valid) of the slot buffers),
+// or none when the debug-bounds build finds them past args.rows.
+__device__ __forceinline__ int checked_rows(const GemmArgs& a, int64_t row0, int n_valid) {
+  if (n_valid > 0 && a.rows > 0 && !NVMOE_BOUNDS(row0 + n_valid <= a.rows, a.status)) return 0;
+  return n_valid;
+}
+
 // Work partition.  With many tiles (>= kStreamKFactor per CTA) CTAs take
 // whole tiles round-robin.  With few tiles (decode) the tiles x K-stages
 // sequence is cut into gridDim.x equal contiguous ranges ("stream-K"): a
@@ -774,8 +781,8 @@ __device__ void requant_own_tile(const GemmArgs& args, const TileInfo& ti, const
   const float denom = __fmul_rn(6.0f, gs);
   const int I = args.I;
   const int k_atoms = (I + kStageK - 1) / kStageK * 4;
-  const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
   const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
+  const int n_valid = checked_rows(args, row0, min(kBM, tb.cnt[ti.e] - ti.mt * kBM));
   const int g_base = ti.nt * 8;                       // 128 columns = 8 blocks
   for (int u = threadIdx.x - 64; u < n_valid * 2; u += 128) {
     const int64_t row = row0 + (u >> 1);
@@ -845,13 +852,15 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
     epi_bar();
     if (!*s_ok) return false;
     tc_fence_after();
-    const bool valid = ti.mt * kBM + row_in_tile < tb.cnt[ti.e];
+    const int tile_valid =
+        checked_rows(args, tb.off[ti.e] + ti.mt * kBM, tb.cnt[ti.e] - ti.mt * kBM);
+    const bool valid = row_in_tile < tile_valid;
     const int64_t row = tb.off[ti.e] + ti.mt * kBM + row_in_tile;
     const int col0 = ti.nt * (args.mode == 1 ? 128 : kBN);
     if (s0 == 0 && s1 == P.k_stages) {
       // whole tile in this CTA: epilogue straight from TMEM.  Valid rows of
       // this warp's quarter (warp-uniform):
-      const int nv_w = min(32, max(0, tb.cnt[ti.e] - ti.mt * kBM - q * 32));
+      const int nv_w = min(32, max(0, tile_valid - q * 32));
       const int64_t qrow0 = tb.off[ti.e] + ti.mt * kBM + q * 32;
       if (args.mode == 1 && nv_w > 0 && nv_w <= kNarrowRows) {
         // few rows (decode): each row's columns spread over the lanes
@@ -916,7 +925,7 @@ __device__ bool run_epilogue(const Phase& P, float gs_a, int E, const Tables& tb
         // of dependent L2 round trips on the few threads that own rows.
         __threadfence();
         if (lead) args.counters[tile] = 0;
-        const int n_valid = min(kBM, tb.cnt[ti.e] - ti.mt * kBM);
+        const int n_valid = min(kBM, tile_valid);
         const int groups = args.mode == 1 ? 32 : 64;   // float4 groups per row
         const int etid = threadIdx.x - 64;
         const int64_t row0 = tb.off[ti.e] + ti.mt * kBM;
@@ -1025,6 +1034,7 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
   const int q = warp & 3;
   const int row_in_tile = q * 32 + lane;
   const bool grouped = args.tap == nullptr;
+  n_valid = checked_rows(args, row0, n_valid);
   const bool valid = row_in_tile < n_valid;
   const int64_t row = row0 + row_in_tile;
   const int nv_w = min(32, max(0, n_valid - q * 32));

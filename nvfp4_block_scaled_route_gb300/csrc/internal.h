@@ -65,7 +65,7 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
                               const int32_t* row_dst, int fanout, const int32_t* row_valid,
                               const float* partial, int n_partial, uint8_t* q,
                               uint8_t* sf_row, uint8_t* sf_mma, float* gs_out,
-                              cudaStream_t stream);
+                              int64_t out_rows, int* status, cudaStream_t stream);
 int quant_amax_blocks(int64_t n_elems);
 
 // ---- expert-parallel dispatch / combine (ep.cu) ----
@@ -77,15 +77,17 @@ cudaError_t launch_ep_pack(const int32_t* ids, const int32_t* padded, const int3
                            int32_t* send_pos, uint8_t* send_rows, int32_t* send_expert,
                            cudaStream_t stream);
 cudaError_t launch_ep_scatter(const uint8_t* rows, int64_t n, int H, const int32_t* slot_of,
-                              uint8_t* xq, uint8_t* xsf, int k_atoms, cudaStream_t stream);
-cudaError_t launch_ep_gather(const void* slot_out, int64_t row_bytes, const int32_t* slot_of,
-                             int64_t n, void* out, cudaStream_t stream);
+                              int64_t out_rows, uint8_t* xq, uint8_t* xsf, int k_atoms,
+                              int* status, cudaStream_t stream);
+cudaError_t launch_ep_gather(const void* slot_out, int64_t row_bytes, int64_t slot_rows,
+                             const int32_t* slot_of, int64_t n, void* out, int* status,
+                             cudaStream_t stream);
 cudaError_t launch_max_reduce(const float* partial, int n, float* out, cudaStream_t stream);
 // Both passes in one CTA, for inputs of at most kQuantSmallElems elements.
 constexpr int64_t kQuantSmallElems = 64 * 1024;
 cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t cols,
                                const int32_t* row_dst, int fanout, uint8_t* q, uint8_t* sf_row,
-                               uint8_t* sf_mma, float* gs_out, cudaStream_t stream);
+                               uint8_t* sf_mma, float* gs_out, int64_t out_rows, int* status, cudaStream_t stream);
 
 // ---- weights ----
 cudaError_t launch_weight_amax(const float* w, int E, int64_t per_expert, float* partial,
@@ -126,6 +128,7 @@ struct GemmArgs {
   float* partials;        // split-tile pieces: [2 * grid][128][256] fp32
   int* counters;          // split-tile arrival counts: [kMaxSplitTiles], zero between calls
   int* status;
+  int64_t rows;           // rows of out / tap / mid_q (checked by the debug-bounds build)
   // Optional: the A operand (activation rows and their scales) is ready once
   // *ready_flag >= ready_value; the producer waits for it (at most
   // ready_limit_ns) before its first load.  nullptr = ready at launch.

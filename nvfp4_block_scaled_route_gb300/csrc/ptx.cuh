@@ -17,6 +17,7 @@ enum : int {
   kErrTimeout = 6,
   kErrBadIndex = 7,
   kErrRange = 8,
+  kErrBounds = 9,
 };
 
 // Upper bound on any single wait inside a kernel (nanoseconds of
@@ -33,6 +34,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void record_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
+
+// In-kernel index checks of the NVMOE_DEBUG_BOUNDS build: a failed check
+// records kErrBounds in the status word (the first code recorded wins) and the
+// caller skips the access; nothing traps.  In the normal build every check is
+// the constant true and compiles away.
+__device__ __forceinline__ bool bounds_ok(bool ok, int* status) {
+  if (!ok) record_status(status, kErrBounds);
+  return ok;
+}
+#ifdef NVMOE_DEBUG_BOUNDS
+#define NVMOE_BOUNDS(cond, status) (::nvmoe::bounds_ok((cond), (status)))
+#else
+#define NVMOE_BOUNDS(cond, status) true
+#endif
 
 // --------------------------------------------------------------- smem ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

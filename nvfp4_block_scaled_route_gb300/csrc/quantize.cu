@@ -80,7 +80,8 @@ __device__ __forceinline__ void pack_rows(const T* __restrict__ x, int64_t rows,
                                           const int32_t* __restrict__ row_dst, int fanout,
                                           const int32_t* __restrict__ row_valid, float gs,
                                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
-                                          uint8_t* __restrict__ sf_mma, int k_atoms) {
+                                          uint8_t* __restrict__ sf_mma, int k_atoms,
+                                          int64_t out_rows, int* status) {
   constexpr int VE = Vec<T>::kElems;
   const float denom = __fmul_rn(6.0f, gs);
   const int bpr = cols >> 4;                       // blocks per row
@@ -118,7 +119,7 @@ __device__ __forceinline__ void pack_rows(const T* __restrict__ x, int64_t rows,
     if (!valid) continue;
     for (int j = 0; j < fanout; ++j) {
       const int64_t dst = row_dst != nullptr ? row_dst[row * fanout + j] : row;
-      if (dst < 0) continue;
+      if (dst < 0 || !NVMOE_BOUNDS(dst < out_rows, status)) continue;
       *reinterpret_cast<uint2*>(q + dst * (cols >> 1) + (int64_t)g * 8) =
           make_uint2(packed[0], packed[1]);
       if (sf_row != nullptr) sf_row[dst * bpr + g] = static_cast<uint8_t>(sf);
@@ -133,7 +134,8 @@ __global__ void __launch_bounds__(kPackThreads) quant_pack_kernel(
     const T* __restrict__ x, int64_t rows, int cols, const int32_t* __restrict__ row_dst,
     int fanout, const int32_t* __restrict__ row_valid, const float* __restrict__ partial,
     int n_partial, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
-    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms) {
+    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms, int64_t out_rows,
+    int* status) {
   __shared__ float s_gs;
   if (threadIdx.x < 32) {
     const float amax = reduce_partials(partial, n_partial);
@@ -144,7 +146,8 @@ __global__ void __launch_bounds__(kPackThreads) quant_pack_kernel(
     }
   }
   __syncthreads();
-  pack_rows<T>(x, rows, cols, row_dst, fanout, row_valid, s_gs, q, sf_row, sf_mma, k_atoms);
+  pack_rows<T>(x, rows, cols, row_dst, fanout, row_valid, s_gs, q, sf_row, sf_mma, k_atoms,
+               out_rows, status);
 }
 
 // Small inputs: amax and quantisation in one CTA (one launch instead of two).
@@ -154,7 +157,8 @@ template <typename T>
 __global__ void __launch_bounds__(kSmallThreads) quant_small_kernel(
     const T* __restrict__ x, int64_t rows, int cols, const int32_t* __restrict__ row_dst,
     int fanout, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
-    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms) {
+    uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms, int64_t out_rows,
+    int* status) {
   constexpr int VE = Vec<T>::kElems;
   __shared__ float s_red[kSmallThreads / 32];
   __shared__ float s_gs;
@@ -178,7 +182,8 @@ __global__ void __launch_bounds__(kSmallThreads) quant_small_kernel(
     }
   }
   __syncthreads();
-  pack_rows<T>(x, rows, cols, row_dst, fanout, nullptr, s_gs, q, sf_row, sf_mma, k_atoms);
+  pack_rows<T>(x, rows, cols, row_dst, fanout, nullptr, s_gs, q, sf_row, sf_mma, k_atoms, out_rows,
+               status);
 }
 
 // ------------------------------------------------------------- weights ----
@@ -304,23 +309,25 @@ cudaError_t launch_quant_amax(const void* x, int x_dtype, int64_t n_elems, float
 
 cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t cols,
                                const int32_t* row_dst, int fanout, uint8_t* q, uint8_t* sf_row,
-                               uint8_t* sf_mma, float* gs_out, cudaStream_t stream) {
+                               uint8_t* sf_mma, float* gs_out, int64_t out_rows, int* status,
+                               cudaStream_t stream) {
   const int k_atoms = static_cast<int>(round_up(cols, kStageK) / 64);
   if (x_dtype == 0)
     quant_small_kernel<__nv_bfloat16><<<1, kSmallThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(x), rows, static_cast<int>(cols), row_dst, fanout, q,
-        sf_row, sf_mma, gs_out, k_atoms);
+        sf_row, sf_mma, gs_out, k_atoms, out_rows, status);
   else
     quant_small_kernel<float><<<1, kSmallThreads, 0, stream>>>(
         static_cast<const float*>(x), rows, static_cast<int>(cols), row_dst, fanout, q, sf_row,
-        sf_mma, gs_out, k_atoms);
+        sf_mma, gs_out, k_atoms, out_rows, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t cols,
                               const int32_t* row_dst, int fanout, const int32_t* row_valid,
                               const float* partial, int n_partial, uint8_t* q, uint8_t* sf_row,
-                              uint8_t* sf_mma, float* gs_out, cudaStream_t stream) {
+                              uint8_t* sf_mma, float* gs_out, int64_t out_rows, int* status,
+                              cudaStream_t stream) {
   const int64_t total = rows * (cols / 16);
   int64_t blocks = ceil_div(total, kPackThreads);
   const int64_t cap = 152 * 16;
@@ -330,11 +337,11 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
   if (x_dtype == 0) {
     quant_pack_kernel<__nv_bfloat16><<<static_cast<int>(blocks), kPackThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(x), rows, static_cast<int>(cols), row_dst, fanout,
-        row_valid, partial, n_partial, q, sf_row, sf_mma, gs_out, k_atoms);
+        row_valid, partial, n_partial, q, sf_row, sf_mma, gs_out, k_atoms, out_rows, status);
   } else {
     quant_pack_kernel<float><<<static_cast<int>(blocks), kPackThreads, 0, stream>>>(
         static_cast<const float*>(x), rows, static_cast<int>(cols), row_dst, fanout, row_valid,
-        partial, n_partial, q, sf_row, sf_mma, gs_out, k_atoms);
+        partial, n_partial, q, sf_row, sf_mma, gs_out, k_atoms, out_rows, status);
   }
   return cudaGetLastError();
 }

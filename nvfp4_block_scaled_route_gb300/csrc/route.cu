@@ -140,6 +140,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(
       continue;
     }
     const int row = base[e] + whist[warp][e] + my_pos[r];
+    if (!NVMOE_BOUNDS(row >= 0 && row < rows_bound, status)) {
+      slot_of[idx] = -1;
+      continue;
+    }
     slot_of[idx] = row;
     row_token[row] = static_cast<int32_t>(idx / k);
   }

@@ -44,6 +44,17 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, fn), fn
 
 
+def test_debug_bounds_library_exports_the_same_symbols(lib):
+    """libnvfp4moe_debug.so (NVMOE_DEBUG_BOUNDS: in-kernel index checks) is
+    built beside the library and loads without a GPU."""
+    path = os.path.join(ROOT, "nvfp4_block_scaled_route_gb300", "libnvfp4moe_debug.so")
+    dbg = ctypes.CDLL(path)
+    for fn in declared_functions():
+        assert hasattr(dbg, fn), fn
+    dbg.nvmoe_status_str.restype = ctypes.c_char_p
+    assert dbg.nvmoe_status_str(9) == b"index outside its buffer (debug-bounds build)"
+
+
 def test_binding_signatures_cover_header(lib):
     from nvfp4_block_scaled_route_gb300 import binding
     assert set(declared_functions()) == set(binding.SIGNATURES)
