@@ -80,6 +80,9 @@ def parse():
     p.add_argument("--part", choices=["layer", "router", "peak"], default="layer",
                    help="the MoE layer (steps 1-7), the router front-end alone, or the "
                         "dense FP4 tensor-core probe alone")
+    p.add_argument("--pdl", choices=["on", "off"], default="off",
+                   help="programmatic dependent launch on the multi-launch path "
+                        "(off by default: measured slower on the prefill step)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
@@ -423,6 +426,7 @@ def main():
     from nvfp4_block_scaled_route_gb300 import binding as nb
     from nvfp4_block_scaled_route_gb300 import synthetic as syn
 
+    nb.lib().nvmoe_set_pdl(1 if args.pdl == "on" else 0)
     cfg = syn.CONFIGS[args.config]
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -728,6 +732,7 @@ def main():
                                     "flush before every step: %.4f)" % flushed_ms) if rotate
                                    else "256 MiB write before every step",
                        "graph": "one CUDA graph per step", "active_experts": E_act,
+                       "pdl": args.pdl,
                        "api": "moe_nvfp4_layer_forward" if args.api == "layer"
                               else "route + quantise + forward + reduce",
                        "gate_up_scales": args.gate_up_scales,

@@ -60,6 +60,7 @@ SIGNATURES = {
     "nvmoe_status_str": (ctypes.c_char_p, [_I]),
     "nvmoe_last_cuda_error": (ctypes.c_char_p, []),
     "nvmoe_version": (_I, []),
+    "nvmoe_set_pdl": (_I, [_I]),
     "nvmoe_kernel_launch_count": (ctypes.c_uint64, []),
     "nvmoe_read_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "nvmoe_clear_status": (_I, [_P, _P]),

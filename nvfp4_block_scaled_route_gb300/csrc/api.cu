@@ -115,6 +115,19 @@ cudaError_t counted(cudaError_t e, int kernels) {
 void nvmoe::note_launches(int kernels) { g_launches += kernels; }
 
 namespace {
+std::atomic<int> g_pdl{0};
+}  // namespace
+
+bool nvmoe::pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
+int nvmoe::pdl_attr(cudaLaunchAttribute* attr) {
+  if (!pdl_enabled()) return 0;
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
+  return 1;
+}
+
+namespace {
 
 // Workspace carving helper.
 struct Carve {
@@ -168,6 +181,11 @@ const char* nvmoe_status_str(int s) {
 }
 
 int nvmoe_version(void) { return 200; }
+
+int nvmoe_set_pdl(int enable) {
+  const int old = g_pdl.exchange(enable != 0 ? 1 : 0);
+  return old;
+}
 
 uint64_t nvmoe_kernel_launch_count(void) { return g_launches.load(); }
 

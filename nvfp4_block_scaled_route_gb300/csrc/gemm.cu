@@ -1275,8 +1275,13 @@ __global__ void __launch_bounds__(kHalf ? kThreadsHalf : kThreadsSt, 1) grouped_
   __shared__ float s_amax[8];
   __shared__ int s_last, s_ok;
 
-  load_tables(tb, args, args.n_tiles);
+  // the next kernel may be scheduled; this one's prologue (barriers, TMEM,
+  // tensor maps) touches no memory of the kernels before it
+  pdl_trigger();
   const uint32_t tmem = setup_cta(bars, &map_a.full, &map_b, &map_a.small, nullptr, kHalf ? 8u : 4u);
+  pdl_wait();
+  load_tables(tb, args, args.n_tiles);
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars->abort;
   Phase P = make_phase(args, &map_a, &map_b, tb.prefix1, args.E);
@@ -1579,7 +1584,7 @@ __global__ void __launch_bounds__(kThreadsHalf, 1) grouped_gemm_pair_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
 
-  load_pair_tables(tb, args);
+  pdl_trigger();
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStagesP; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -1604,6 +1609,8 @@ __global__ void __launch_bounds__(kThreadsHalf, 1) grouped_gemm_pair_kernel(
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
+  pdl_wait();
+  load_pair_tables(tb, args);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -2207,36 +2214,39 @@ cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensor
   // over CTA pairs when the grid holds at least one pair.
   const bool half = min_tiles >= int64_t{kStreamKFactor} * grid &&
                     !(args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue);
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
   if (half && allow_pair && grid >= 2) {
     const cudaError_t err = set_smem_attr_once(
         g_gemm_pair_attr, reinterpret_cast<const void*>(grouped_gemm_pair_kernel), kSmemBytesP);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid & ~1);
     cfg.blockDim = dim3(kThreadsHalf);
     cfg.dynamicSmemBytes = kSmemBytesP;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1 + pdl_attr(&attr[1]);
     return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, map_a, map_b, args);
   }
+  cfg.gridDim = dim3(grid);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.numAttrs = pdl_attr(&attr[0]);
   if (half) {
     const cudaError_t err = set_smem_attr_once(
         g_gemm_half_attr, reinterpret_cast<const void*>(grouped_gemm_kernel<true>), kSmemBytes);
     if (err != cudaSuccess) return err;
-    grouped_gemm_kernel<true><<<grid, kThreadsHalf, kSmemBytes, stream>>>(map_a, map_b, args);
-    return cudaGetLastError();
+    cfg.blockDim = dim3(kThreadsHalf);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true>, map_a, map_b, args);
   }
   const cudaError_t err = set_smem_attr_once(
       g_gemm_attr, reinterpret_cast<const void*>(grouped_gemm_kernel<false>), kSmemBytes);
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<false><<<grid, kThreadsSt, kSmemBytes, stream>>>(map_a, map_b, args);
-  return cudaGetLastError();
+  cfg.blockDim = dim3(kThreadsSt);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false>, map_a, map_b, args);
 }
 
 cudaError_t launch_fused_ffn(const GemmArgs& a1, const GemmArgs& a2, const AMaps& map_x,

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace nvmoe {
 
@@ -67,6 +68,30 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
                               uint8_t* sf_row, uint8_t* sf_mma, float* gs_out,
                               int64_t out_rows, int* status, cudaStream_t stream);
 int quant_amax_blocks(int64_t n_elems);
+
+// ---- programmatic dependent launch ----
+// Whether the step kernels of the multi-launch path are launched with
+// programmatic stream serialization (nvmoe_set_pdl; default off), and the
+// launch attribute that does it (attr count 0 or 1 written into attr[]).
+bool pdl_enabled();
+int pdl_attr(cudaLaunchAttribute* attr);
+
+// kernel<<<grid, block, smem, stream>>>(args...) with the PDL attribute when
+// enabled; the kernel must call pdl_wait() before touching memory of earlier
+// kernels.  Errors as for any launch (also left for cudaGetLastError).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(attr);
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- expert-parallel dispatch / combine (ep.cu) ----
 cudaError_t launch_ep_dest(const int32_t* ids, int64_t S, int E, int G, int32_t* dest, int* status,

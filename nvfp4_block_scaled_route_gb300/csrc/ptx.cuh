@@ -49,6 +49,21 @@ __device__ __forceinline__ bool bounds_ok(bool ok, int* status) {
 #define NVMOE_BOUNDS(cond, status) true
 #endif
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while the
+// kernel before it in the stream is still running.  pdl_wait(): every thread
+// waits until that kernel has completed and its writes are visible; executed
+// before the first access to memory the earlier kernels touch.
+// pdl_trigger(): lets the next kernel in the stream be scheduled (it waits in
+// its own pdl_wait).  Both are no-ops in a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- smem ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

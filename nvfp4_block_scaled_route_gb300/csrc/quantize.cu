@@ -53,6 +53,8 @@ template <typename T>
 __global__ void __launch_bounds__(kAmaxThreads) quant_amax_kernel(const T* __restrict__ x,
                                                                    int64_t n_vec,
                                                                    float* __restrict__ partial) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int VE = Vec<T>::kElems;
   float m = 0.0f;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_vec;
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(kPackThreads) quant_pack_kernel(
     int n_partial, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
     uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms, int64_t out_rows,
     int* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s_gs;
   if (threadIdx.x < 32) {
     const float amax = reduce_partials(partial, n_partial);
@@ -159,6 +163,8 @@ __global__ void __launch_bounds__(kSmallThreads) quant_small_kernel(
     int fanout, uint8_t* __restrict__ q, uint8_t* __restrict__ sf_row,
     uint8_t* __restrict__ sf_mma, float* __restrict__ gs_out, int k_atoms, int64_t out_rows,
     int* status) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int VE = Vec<T>::kElems;
   __shared__ float s_red[kSmallThreads / 32];
   __shared__ float s_gs;
@@ -298,10 +304,10 @@ int quant_amax_blocks(int64_t n_elems) {
 cudaError_t launch_quant_amax(const void* x, int x_dtype, int64_t n_elems, float* partial,
                               int n_partial, cudaStream_t stream) {
   if (x_dtype == 0) {
-    quant_amax_kernel<__nv_bfloat16><<<n_partial, kAmaxThreads, 0, stream>>>(
+    (void)launch_pdl(quant_amax_kernel<__nv_bfloat16>, dim3(n_partial), dim3(kAmaxThreads), 0, stream, 
         static_cast<const __nv_bfloat16*>(x), n_elems / 8, partial);
   } else {
-    quant_amax_kernel<float><<<n_partial, kAmaxThreads, 0, stream>>>(
+    (void)launch_pdl(quant_amax_kernel<float>, dim3(n_partial), dim3(kAmaxThreads), 0, stream, 
         static_cast<const float*>(x), n_elems / 4, partial);
   }
   return cudaGetLastError();
@@ -313,11 +319,11 @@ cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t
                                cudaStream_t stream) {
   const int k_atoms = static_cast<int>(round_up(cols, kStageK) / 64);
   if (x_dtype == 0)
-    quant_small_kernel<__nv_bfloat16><<<1, kSmallThreads, 0, stream>>>(
+    (void)launch_pdl(quant_small_kernel<__nv_bfloat16>, dim3(1), dim3(kSmallThreads), 0, stream, 
         static_cast<const __nv_bfloat16*>(x), rows, static_cast<int>(cols), row_dst, fanout, q,
         sf_row, sf_mma, gs_out, k_atoms, out_rows, status);
   else
-    quant_small_kernel<float><<<1, kSmallThreads, 0, stream>>>(
+    (void)launch_pdl(quant_small_kernel<float>, dim3(1), dim3(kSmallThreads), 0, stream, 
         static_cast<const float*>(x), rows, static_cast<int>(cols), row_dst, fanout, q, sf_row,
         sf_mma, gs_out, k_atoms, out_rows, status);
   return cudaGetLastError();
@@ -335,11 +341,11 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
   if (blocks < 1) blocks = 1;
   const int k_atoms = static_cast<int>(round_up(cols, kStageK) / 64);
   if (x_dtype == 0) {
-    quant_pack_kernel<__nv_bfloat16><<<static_cast<int>(blocks), kPackThreads, 0, stream>>>(
+    (void)launch_pdl(quant_pack_kernel<__nv_bfloat16>, dim3(static_cast<int>(blocks)), dim3(kPackThreads), 0, stream, 
         static_cast<const __nv_bfloat16*>(x), rows, static_cast<int>(cols), row_dst, fanout,
         row_valid, partial, n_partial, q, sf_row, sf_mma, gs_out, k_atoms, out_rows, status);
   } else {
-    quant_pack_kernel<float><<<static_cast<int>(blocks), kPackThreads, 0, stream>>>(
+    (void)launch_pdl(quant_pack_kernel<float>, dim3(static_cast<int>(blocks)), dim3(kPackThreads), 0, stream, 
         static_cast<const float*>(x), rows, static_cast<int>(cols), row_dst, fanout, row_valid,
         partial, n_partial, q, sf_row, sf_mma, gs_out, k_atoms, out_rows, status);
   }

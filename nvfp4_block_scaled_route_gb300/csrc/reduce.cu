@@ -35,6 +35,8 @@ template <typename TIn, bool kBf16>
 __global__ void __launch_bounds__(kReduceThreads) unpermute_reduce_kernel(
     const TIn* __restrict__ slot_out, const int32_t* __restrict__ slot_of,
     const float* __restrict__ topk_w, int64_t T, int k, int64_t H, void* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_slot[kMaxTopK];
   __shared__ float s_w[kMaxTopK];
   const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
@@ -82,17 +84,17 @@ cudaError_t launch_reduce(const void* slot_out, int slot_dtype, const int32_t* s
   const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(slot_out);
   const __half* h = static_cast<const __half*>(slot_out);
   if (slot_dtype == 2 && y_dtype == 0)
-    unpermute_reduce_kernel<__half, true><<<grid, kReduceThreads, 0, stream>>>(h, slot_of, topk_w, T, k, H, y);
+    (void)launch_pdl(unpermute_reduce_kernel<__half, true>, dim3(grid), dim3(kReduceThreads), 0, stream, h, slot_of, topk_w, T, k, H, y);
   else if (slot_dtype == 2)
-    unpermute_reduce_kernel<__half, false><<<grid, kReduceThreads, 0, stream>>>(h, slot_of, topk_w, T, k, H, y);
+    (void)launch_pdl(unpermute_reduce_kernel<__half, false>, dim3(grid), dim3(kReduceThreads), 0, stream, h, slot_of, topk_w, T, k, H, y);
   else if (slot_dtype == 1 && y_dtype == 0)
-    unpermute_reduce_kernel<float, true><<<grid, kReduceThreads, 0, stream>>>(f, slot_of, topk_w, T, k, H, y);
+    (void)launch_pdl(unpermute_reduce_kernel<float, true>, dim3(grid), dim3(kReduceThreads), 0, stream, f, slot_of, topk_w, T, k, H, y);
   else if (slot_dtype == 1)
-    unpermute_reduce_kernel<float, false><<<grid, kReduceThreads, 0, stream>>>(f, slot_of, topk_w, T, k, H, y);
+    (void)launch_pdl(unpermute_reduce_kernel<float, false>, dim3(grid), dim3(kReduceThreads), 0, stream, f, slot_of, topk_w, T, k, H, y);
   else if (y_dtype == 0)
-    unpermute_reduce_kernel<__nv_bfloat16, true><<<grid, kReduceThreads, 0, stream>>>(b, slot_of, topk_w, T, k, H, y);
+    (void)launch_pdl(unpermute_reduce_kernel<__nv_bfloat16, true>, dim3(grid), dim3(kReduceThreads), 0, stream, b, slot_of, topk_w, T, k, H, y);
   else
-    unpermute_reduce_kernel<__nv_bfloat16, false><<<grid, kReduceThreads, 0, stream>>>(b, slot_of, topk_w, T, k, H, y);
+    (void)launch_pdl(unpermute_reduce_kernel<__nv_bfloat16, false>, dim3(grid), dim3(kReduceThreads), 0, stream, b, slot_of, topk_w, T, k, H, y);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,8 @@ constexpr int kRounds = kPerWarp / 32;
 __global__ void __launch_bounds__(kRouteThreads) route_count_kernel(
     const int32_t* __restrict__ ids, int64_t S, int E, int32_t* __restrict__ chunk_counts,
     int32_t* __restrict__ row_token, int64_t rows_bound, int* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -47,6 +49,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(
     const int32_t* __restrict__ chunk_counts, int n_chunks, int32_t* __restrict__ expert_offsets,
     int32_t* __restrict__ expert_counts, int32_t* __restrict__ row_token,
     int32_t* __restrict__ slot_of, int64_t rows_bound, int* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int base[kMaxExperts];        // first row of this chunk's slots per expert
   __shared__ int total[kMaxExperts];
   __shared__ int whist[kWarps][kMaxExperts];
@@ -160,16 +164,16 @@ cudaError_t launch_route(const int32_t* topk_ids, int64_t T, int k, int E,
   const int64_t S = T * k;
   if (n_chunks == 1) {
     // one chunk: histogram, prefix sum and assignment in a single CTA
-    route_assign_kernel<<<1, kRouteThreads, 0, stream>>>(topk_ids, S, k, E, nullptr, 1,
+    (void)launch_pdl(route_assign_kernel, dim3(1), dim3(kRouteThreads), 0, stream, topk_ids, S, k, E, nullptr, 1,
                                                          expert_offsets, expert_counts,
                                                          row_token, slot_of, rows_bound, status);
     return cudaGetLastError();
   }
-  route_count_kernel<<<n_chunks, kRouteThreads, 0, stream>>>(topk_ids, S, E, chunk_counts,
+  (void)launch_pdl(route_count_kernel, dim3(n_chunks), dim3(kRouteThreads), 0, stream, topk_ids, S, E, chunk_counts,
                                                              row_token, rows_bound, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  route_assign_kernel<<<n_chunks, kRouteThreads, 0, stream>>>(
+  (void)launch_pdl(route_assign_kernel, dim3(n_chunks), dim3(kRouteThreads), 0, stream, 
       topk_ids, S, k, E, chunk_counts, n_chunks, expert_offsets, expert_counts, row_token,
       slot_of, rows_bound, status);
   return cudaGetLastError();

@@ -518,6 +518,45 @@ def test_layer_staged_host_step(nb):
     assert torch.equal(out, y_dev)
 
 
+def test_programmatic_dependent_launch_changes_nothing(nb):
+    """The multi-launch path (route, quantise, L1, requantise, L2, reduce:
+    the waves workload through the one-call layer) with programmatic
+    dependent launch on and off, eager and replayed from a CUDA graph: the
+    same bits (every kernel waits for the one before it before touching its
+    memory)."""
+    cfg = syn.CONFIGS["waves"]
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e, device=DEV) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e, device=DEV) for e in range(cfg.E)])
+    q1, s1, g1 = nb.quantize_weights(W1)
+    q2, s2, g2 = nb.quantize_weights(W2)
+    pw = nb.PreparedWeights.from_checkpoint(q1, s1, g1, q2, s2, g2)
+    layer = nb.FusedLayer(pw, cfg.T, cfg.k, device=DEV)
+    x = syn.draw_activations(cfg).to(DEV)
+    ids, w = syn.draw_routing(cfg)
+    ids, w = ids.to(DEV), w.to(DEV)
+    outs = []
+    prev = nb.lib().nvmoe_set_pdl(0)
+    try:
+        for pdl in (0, 1):
+            nb.lib().nvmoe_set_pdl(pdl)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                outs.append(layer.forward(x, ids, w).clone())
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    layer.forward(x, ids, w)
+                layer.y.zero_()
+                for _ in range(3):
+                    g.replay()
+            s.synchronize()
+            outs.append(layer.y.clone())
+            assert layer.status() == 0
+    finally:
+        nb.lib().nvmoe_set_pdl(prev)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
 @pytest.mark.parametrize("name", ["small", "waves"])
 def test_staged_pipeline_overlapped_steps(nb, name):
     """StagedPipeline: two slots with different inputs, seven steps whose
