@@ -226,7 +226,13 @@ int moe_route_permute_noalloc(const int32_t* topk_ids, int64_t T, int k, int E,
  *   sf_rowmajor  optional uint8 [out_rows, cols/16] scale bytes, row-major.
  *   sf_mma       optional staged scales, nvfp4_sf_mma_bytes(out_rows, cols).
  *   gs_out       float [1]: gs.
- * Output rows not written by any input row are left untouched.
+ * Output rows not written by any input row are left untouched, except that
+ * when both scale layouts are given (cols % 256 == 0, sf_rowmajor 16-byte
+ * aligned, rows * cols > 65536) the staged scales are written
+ * by a second pass over sf_rowmajor: every 128-row tile of sf_mma is then
+ * rewritten whole, an unwritten row's staged bytes being whatever its
+ * sf_rowmajor row holds (zero past out_rows).  The bytes of written rows are
+ * the same either way.
  * Limits: cols % 64 == 0, 1 <= fanout <= 32.  rows = 0 writes gs = 1.
  */
 size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t cols);

@@ -110,6 +110,11 @@ cudaError_t launch_ep_gather(const void* slot_out, int64_t row_bytes, int64_t sl
 cudaError_t launch_max_reduce(const float* partial, int n, float* out, cudaStream_t stream);
 // Both passes in one CTA, for inputs of at most kQuantSmallElems elements.
 constexpr int64_t kQuantSmallElems = 64 * 1024;
+// Row-major activation scales (cols % 256 == 0, 16-byte aligned) into the
+// staged layout, rows rounded up to whole 128-row tiles (rows past `rows`
+// get zero scales).
+cudaError_t launch_stage_act_sf(const uint8_t* sf_row, int64_t rows, int64_t cols,
+                                uint8_t* sf_mma, cudaStream_t stream);
 cudaError_t launch_quant_small(const void* x, int x_dtype, int64_t rows, int64_t cols,
                                const int32_t* row_dst, int fanout, uint8_t* q, uint8_t* sf_row,
                                uint8_t* sf_mma, float* gs_out, int64_t out_rows, int* status, cudaStream_t stream);

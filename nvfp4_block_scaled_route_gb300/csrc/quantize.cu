@@ -352,6 +352,50 @@ cudaError_t launch_quant_pack(const void* x, int x_dtype, int64_t rows, int64_t 
   return cudaGetLastError();
 }
 
+// Row-major activation scales [rows, cols/16] -> the staged layout, one CTA
+// per 128-row tile.  Atom kb of tile mt holds in its 16-byte row i the four
+// scale bytes of k-block kb of rows 32j + i (j = 0..3, word j); a lane reads
+// the 16 bytes of four k-blocks of its four rows and writes one 16-byte atom
+// row per k-block, so every load and store is a full 16 bytes and a warp's
+// stores cover whole 512-byte atoms.  Rows at or past `rows` read as zero.
+// (The quantiser's own staged writes are 4-byte words whose sectors are
+// completed by other tokens' rows much later; this pass replaces them.)
+__global__ void __launch_bounds__(kPackThreads) stage_act_sf_kernel(
+    const uint8_t* __restrict__ sf_row, int64_t rows, int bpr, uint8_t* __restrict__ sf_mma,
+    int k_atoms) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t mt = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_quads = bpr / 16;
+  for (int c = warp; c < n_quads; c += kPackThreads / 32) {
+    uint32_t v[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = mt * kTileRows + 32 * j + lane;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) u = __ldg(reinterpret_cast<const uint4*>(sf_row + r * bpr) + c);
+      v[j][0] = u.x; v[j][1] = u.y; v[j][2] = u.z; v[j][3] = u.w;
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint4* dst = reinterpret_cast<uint4*>(
+          sf_mma + (static_cast<size_t>(mt) * k_atoms + 4 * c + w) * kSfAtomBytes) + lane;
+      *dst = make_uint4(v[0][w], v[1][w], v[2][w], v[3][w]);
+    }
+  }
+}
+
+cudaError_t launch_stage_act_sf(const uint8_t* sf_row, int64_t rows, int64_t cols,
+                                uint8_t* sf_mma, cudaStream_t stream) {
+  const int64_t tiles = ceil_div(rows, kTileRows);
+  if (tiles == 0) return cudaSuccess;
+  const int k_atoms = static_cast<int>(round_up(cols, kStageK) / 64);
+  (void)launch_pdl(stage_act_sf_kernel, dim3(static_cast<unsigned>(tiles)), dim3(kPackThreads), 0,
+                   stream, sf_row, rows, static_cast<int>(cols / 16), sf_mma, k_atoms);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_weight_amax(const float* w, int E, int64_t per_expert, float* partial,
                                int parts_per_expert, cudaStream_t stream) {
   dim3 grid(parts_per_expert, E);

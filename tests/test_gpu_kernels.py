@@ -158,21 +158,29 @@ def test_quantize_act_empty_and_zero(nb):
     assert gs.item() == 1.0
 
 
-def test_quantize_scatter_into_slot_layout(nb):
-    cfg = syn.CONFIGS["small"]
+@pytest.mark.parametrize("name,rowmajor", [("small", False), ("medium", False),
+                                           ("medium", True), ("waves", True)])
+def test_quantize_scatter_into_slot_layout(nb, name, rowmajor):
+    """Token rows quantised into their k slot rows.  With both scale layouts
+    asked for (and more than the single-CTA size), the staged scales come
+    from a second pass over the row-major ones: both must match the oracle
+    on every slot row, whatever the padding rows hold."""
+    cfg = syn.CONFIGS[name]
     x = syn.draw_activations(cfg)
     ids, _ = syn.draw_routing(cfg)
     r = nb.route_permute(ids.to(DEV), cfg.E)
-    q, _, sf_mma, gs = nb.quantize_act(x.to(DEV), row_dst=r.slot_of, fanout=cfg.k,
-                                       out_rows=r.rows, rowmajor_sf=False)
+    q, sf_row, sf_mma, gs = nb.quantize_act(x.to(DEV), row_dst=r.slot_of, fanout=cfg.k,
+                                            out_rows=r.rows, rowmajor_sf=rowmajor)
     xq, xsf, xgs = onv.quantize_rows(x.float().numpy())
     slot_of = r.slot_of.cpu().numpy().reshape(cfg.T, cfg.k)
     qn = q.cpu().numpy()
     sfn = unstage(sf_mma.cpu().numpy(), r.rows, cfg.H)
-    for t in range(cfg.T):
-        for j in range(cfg.k):
-            assert np.array_equal(qn[slot_of[t, j]], xq[t])
-            assert np.array_equal(sfn[slot_of[t, j]], xsf[t])
+    rows = slot_of.reshape(-1)
+    tok = np.repeat(np.arange(cfg.T), cfg.k)
+    assert np.array_equal(qn[rows], xq[tok])
+    assert np.array_equal(sfn[rows], xsf[tok])
+    if rowmajor:
+        assert np.array_equal(sf_row.cpu().numpy()[rows], xsf[tok])
     assert gs.item() == float(xgs)
 
 
