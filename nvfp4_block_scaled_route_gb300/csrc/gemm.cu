@@ -697,7 +697,9 @@ __device__ bool run_sf_writer(const Phase& P, Barriers* bars, uint8_t* smem, uin
 // Top-k weighted reduce done inside the layer kernel: when the last of a
 // token's k slot rows of one 256-column tile of slot_out is written, the
 // CTA that wrote it sums the k rows (ascending j, fp32, the same arithmetic
-// as unpermute_reduce_kernel) into y.
+// as unpermute_reduce_kernel) into y.  A slot with no row (an expert id
+// outside [0, E)) is counted in advance by CTA 0 and not summed, as in
+// unpermute_reduce_kernel.
 struct YReduce {
   int* counts;              // [T][n_tiles], zero between calls
   const float* topk_w;      // [T, k]
@@ -738,17 +740,19 @@ __device__ void y_after_tile(const YReduce& yr, const TileInfo& ti, const Tables
     for (int j0 = 0; j0 < yr.k; j0 += 8) {
       float4 v[8];
       float wj[8];
+      uint32_t live = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (j0 + j < yr.k) {
-          const int s = yr.slot_row[t * yr.k + j0 + j];
+        const int s = j0 + j < yr.k ? yr.slot_row[t * yr.k + j0 + j] : -1;
+        if (s >= 0) {
           v[j] = __ldcg(reinterpret_cast<const float4*>(args.out + static_cast<int64_t>(s) * H + col));
           wj[j] = __ldg(yr.topk_w + t * yr.k + j0 + j);
+          live |= 1u << j;
         }
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (j0 + j < yr.k) {
+        if ((live >> j) & 1u) {
           acc.x = __fmaf_rn(wj[j], v[j].x, acc.x);
           acc.y = __fmaf_rn(wj[j], v[j].y, acc.y);
           acc.z = __fmaf_rn(wj[j], v[j].z, acc.z);
@@ -1798,7 +1802,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
 //    h); then h is requantised the same way, a 1/G share per CTA, and the
 //    L2 activation loads wait for the second count;
 //  * the top-k reduce of a (token, 256-column tile) is done by the CTA that
-//    writes the last of the token's k slot rows of that tile.
+//    writes the last of the token's k slot rows of that tile (slots with no
+//    row counted in advance by CTA 0).
 // Work per CTA before each wait is one or two rounds of 16-element blocks
 // per thread: on a small batch the critical path is a handful of memory
 // round trips, not a loop over whole rows.
@@ -2116,7 +2121,26 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     if (blockIdx.x == 0) {
       for (int i = etid; i < S; i += 128) {
         L.slot_of[i] = s_row[i];
-        if (s_row[i] >= 0) L.row_token[s_row[i]] = i / k;
+        if (s_row[i] >= 0) {
+          L.row_token[s_row[i]] = i / k;
+        } else {
+          // an expert id outside [0, E): no L2 tile will count this slot, so
+          // it is counted now (the grid barrier orders this before every L2
+          // epilogue); a token without any valid slot gets y = 0
+          const int t = i / k;
+          bool any = false;
+          for (int j = 0; j < k; ++j) any |= s_row[t * k + j] >= 0;
+          if (any) {
+            for (int nt = 0; nt < a2.n_tiles; ++nt) atomicAdd(&L.ycnt[t * a2.n_tiles + nt], 1);
+          } else if (i == t * k) {
+            for (int c = 0; c < H; ++c) {
+              if (L.y_dtype == 0)
+                static_cast<__nv_bfloat16*>(L.y)[static_cast<int64_t>(t) * H + c] = __float2bfloat16(0.0f);
+              else
+                static_cast<float*>(L.y)[static_cast<int64_t>(t) * H + c] = 0.0f;
+            }
+          }
+        }
       }
     }
     quantise_share<true>(L.x, L.T, H, k, s_row, L.xq, L.xsf, s_gs);

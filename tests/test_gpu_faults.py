@@ -118,3 +118,32 @@ def test_layer_forward_rejects_ready_flag(nb):
     with pytest.raises(nb.NvmoeError) as e:
         layer.forward(x, ids.to(DEV), w.to(DEV), taps={"ready_flag": flag, "ready_value": 1})
     assert e.value.status == ERR_INVALID_ARG
+
+
+def test_layer_kernel_bad_expert_ids(nb):
+    """The single-kernel layer with expert ids outside [0, E): the dropped
+    choices take no part in the top-k reduce, exactly as in the four-call
+    path (the same bits of y), a token none of whose choices is valid gets
+    y = 0, and the status word reports NVMOE_ERR_DEVICE_BAD_INDEX."""
+    cfg = syn.MoEConfig("layer_bad", E=8, H=512, I=256, T=6, k=4, routing="uniform")
+    pw = _layer(nb, cfg)
+    x = syn.draw_activations(cfg).to(DEV)
+    ids, w = syn.draw_routing(cfg)
+    ids[1, 2] = cfg.E + 1
+    ids[4, :] = -1
+    ids, w = ids.to(DEV), w.to(DEV)
+    fl = nb.FusedLayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=torch.float32)
+    fl.y.fill_(7.0)
+    outs = []
+    for _ in range(2):               # the self-clearing counters, once more
+        y = fl.forward(x, ids, w, taps={"path": nb.PATH_LAYER}).clone()
+        torch.cuda.synchronize()
+        outs.append(y.cpu())
+    assert nb.read_status(fl.ws) == ERR_BAD_INDEX
+    assert torch.equal(outs[0], outs[1])
+    ref = nb.MoELayer(pw, cfg.T, cfg.k, device=DEV, out_dtype=torch.float32)
+    y_ref = ref.forward(x, ids, w, taps={"path": nb.PATH_SEPARATE}).cpu()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[1], y_ref)
+    assert torch.all(outs[1][4] == 0)
+    assert torch.all(outs[1][1] != 7.0)
