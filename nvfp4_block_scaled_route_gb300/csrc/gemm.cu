@@ -1136,6 +1136,46 @@ __device__ __forceinline__ void epi_tile_half(const GemmArgs& args, int nt, int 
   }
 }
 
+// With a static intermediate scale (two-set epilogues): this set requantises
+// the 64 h columns of the tile it has just stored, for the tile's valid rows,
+// with the expert's gs_mid: four 16-element blocks and one staged scale word
+// per row, re-read from L2 once every store of the set has been made (one
+// row per thread; the same block arithmetic as every other quantisation).
+// The L1 epilogue has the slack for it: a tile's MMAs take far longer.
+__device__ __noinline__ void requant_set_cols(const GemmArgs& args, int nt, int n_valid,
+                                              int64_t row0, float gs, int set) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (set == 0)
+    asm volatile("bar.sync 3, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 4, 128;" ::: "memory");
+  n_valid = checked_rows(args, row0, n_valid);
+  const int r = (warp & 3) * 32 + lane;
+  if (r < n_valid) {
+    const float denom = __fmul_rn(6.0f, gs);
+    const int I = args.I;
+    const int k_atoms = (I + kStageK - 1) / kStageK * 4;
+    const int64_t row = row0 + r;
+    const int g0 = nt * 8 + set * 4;
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float4* p = reinterpret_cast<const float4*>(args.out + row * I + (g0 + b) * 16);
+      float v[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 f = __ldcg(p + c);
+        v[4 * c] = f.x; v[4 * c + 1] = f.y; v[4 * c + 2] = f.z; v[4 * c + 3] = f.w;
+      }
+      uint32_t packed[2];
+      word |= quant_block16(v, gs, denom, packed) << (8 * b);
+      *reinterpret_cast<uint2*>(args.mid_q + row * (I / 2) + (g0 + b) * 8) =
+          make_uint2(packed[0], packed[1]);
+    }
+    *reinterpret_cast<uint32_t*>(args.mid_sf + staged_offset(row, g0, k_atoms)) = word;
+  }
+}
+
 __device__ bool run_epilogue_half(const Phase& P, float gs_a, int E, const Tables& tb,
                                   Barriers* bars, uint32_t tmem, volatile int* abort,
                                   float& amax) {
@@ -1545,6 +1585,10 @@ __device__ bool run_sf_writer_pair(const GemmArgs& args, const PairTables& tb, B
   return true;
 }
 
+// kMidOwn: L1 with a static intermediate scale requantised by the epilogue
+// sets (a separate instantiation, so that the common path keeps its
+// register allocation).
+template <bool kMidOwn>
 __device__ bool run_epilogue_pair(const GemmArgs& args, const PairTables& tb, BarriersP* bars,
                                   uint32_t tmem, uint32_t rank, volatile int* abort,
                                   float& amax) {
@@ -1572,11 +1616,15 @@ __device__ bool run_epilogue_pair(const GemmArgs& args, const PairTables& tb, Ba
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(acc_empty0);
                   });
+    if (kMidOwn)
+      requant_set_cols(args, pt.nt, n_valid, tb.off[pt.e] + pt.m * kBM,
+                       __ldg(args.gs_mid + pt.e), set);
     acc_phase ^= 1u;
   }
   return true;
 }
 
+template <bool kMidOwn>
 __global__ void __launch_bounds__(kThreadsHalf, 1) grouped_gemm_pair_kernel(
     const __grid_constant__ AMaps map_a, const __grid_constant__ CUtensorMap map_b,
     const GemmArgs args) {
@@ -1641,7 +1689,7 @@ __global__ void __launch_bounds__(kThreadsHalf, 1) grouped_gemm_pair_kernel(
     run_sf_writer_pair(args, tb, bars, smem, tmem, abort);
   } else {
     float amax = 0.0f;
-    run_epilogue_pair(args, tb, bars, tmem, rank, abort, amax);
+    run_epilogue_pair<kMidOwn>(args, tb, bars, tmem, rank, abort, amax);
     if (args.mode == 1) publish_amax_half(amax, s_amax, args.amax_partial);
   }
   // the pair's MMAs read both CTAs' shared memory and TMEM: neither leaves
@@ -2200,7 +2248,8 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
   }
 }
 
-PerDeviceOnce g_gemm_attr, g_gemm_half_attr, g_gemm_pair_attr, g_fused_attr, g_layer_attr;
+PerDeviceOnce g_gemm_attr, g_gemm_half_attr, g_gemm_pair_attr, g_gemm_pair_mid_attr, g_fused_attr,
+    g_layer_attr;
 
 }  // namespace
 
@@ -2233,18 +2282,23 @@ int gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensorMap& map_b,
                         int grid, int64_t min_tiles, bool allow_pair, cudaStream_t stream) {
-  // At least kStreamKFactor tiles per CTA whatever the routing, and no
-  // requantisation inside the epilogue: whole tiles and two epilogue sets,
-  // over CTA pairs when the grid holds at least one pair.
-  const bool half = min_tiles >= int64_t{kStreamKFactor} * grid &&
-                    !(args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue);
+  // At least kStreamKFactor tiles per CTA whatever the routing: whole tiles
+  // and two epilogue sets, over CTA pairs when the grid holds at least one
+  // pair.  A static intermediate scale requantised in the L1 epilogue takes
+  // the pair kernel's own instantiation (each set requantises the columns
+  // it stored), else the one-CTA kernel.
+  const bool mid_own = args.mode == 1 && args.gs_mid != nullptr && args.mid_in_epilogue;
+  const bool pair = min_tiles >= int64_t{kStreamKFactor} * grid && allow_pair && grid >= 2;
+  const bool half = min_tiles >= int64_t{kStreamKFactor} * grid && !mid_own;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  if (half && allow_pair && grid >= 2) {
-    const cudaError_t err = set_smem_attr_once(
-        g_gemm_pair_attr, reinterpret_cast<const void*>(grouped_gemm_pair_kernel), kSmemBytesP);
+  if (pair) {
+    const void* kernel = mid_own ? reinterpret_cast<const void*>(grouped_gemm_pair_kernel<true>)
+                                 : reinterpret_cast<const void*>(grouped_gemm_pair_kernel<false>);
+    const cudaError_t err =
+        set_smem_attr_once(mid_own ? g_gemm_pair_mid_attr : g_gemm_pair_attr, kernel, kSmemBytesP);
     if (err != cudaSuccess) return err;
     cfg.gridDim = dim3(grid & ~1);
     cfg.blockDim = dim3(kThreadsHalf);
@@ -2254,7 +2308,8 @@ cudaError_t launch_gemm(const GemmArgs& args, const AMaps& map_a, const CUtensor
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.numAttrs = 1 + pdl_attr(&attr[1]);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, map_a, map_b, args);
+    if (mid_own) return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<true>, map_a, map_b, args);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<false>, map_a, map_b, args);
   }
   cfg.gridDim = dim3(grid);
   cfg.dynamicSmemBytes = kSmemBytes;

@@ -599,11 +599,14 @@ def test_staged_pipeline_overlapped_steps(nb, name):
 # ------------------------------------------ static intermediate scale ----
 
 @pytest.mark.parametrize("name,path", [("tiny", 1), ("tiny", 2), ("tiny", 3),
-                                       ("small", 1), ("small", 2), ("medium", 1)])
+                                       ("small", 1), ("small", 2), ("medium", 1),
+                                       ("waves", 1)])
 def test_forward_static_mid_scale(nb, name, path):
     """A static intermediate scale per expert: each CTA requantises its own
     L1 tiles with gs_mid[e] (no global amax, no requantisation pass); L2
-    alpha gs_mid[e]*gs_w2[e].  Scales span saturating and coarse cases."""
+    alpha gs_mid[e]*gs_w2[e].  Scales span saturating and coarse cases.
+    At the waves size the L1 GEMM takes whole tiles on CTA pairs, where each
+    epilogue set requantises the columns it has stored."""
     cfg = syn.CONFIGS[name]
     x = syn.draw_activations(cfg)
     ids, w = syn.draw_routing(cfg)
