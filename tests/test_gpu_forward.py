@@ -420,10 +420,13 @@ def test_layer_kernel_equals_four_calls(nb, cfg, out_dtype):
     assert np.array_equal(a["y"], b["y"])
 
 
-def test_layer_forward_large_batch_uses_four_launches(nb):
+@pytest.mark.parametrize("name", ["small", "waves"])
+def test_layer_forward_large_batch_uses_four_launches(nb, name):
     """Above the single-kernel limits the one-call API runs the four steps
-    (with fp16 slot rows): the same bits as the four calls made directly."""
-    cfg = syn.CONFIGS["small"]                       # T*k = 291 > 128
+    (with fp16 slot rows): the same bits as the four calls made directly,
+    with the L1 GEMM on the stream-K kernel (small) and on CTA pairs
+    (waves)."""
+    cfg = syn.CONFIGS[name]                          # T*k = 291 / 9856 > 128
     x = syn.draw_activations(cfg)
     ids, w = syn.draw_routing(cfg)
     W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)]).to(DEV)
