@@ -1,4 +1,6 @@
-// Top-k weighted gather-reduce back to token order:
+// Top-k weighted gather-reduce back to token order ("NVFP4 MegaMoE Debug
+// Log", NVFP4 MoE Pipeline: the scatter of the L2 outputs with the routing
+// weights):
 //   y[t, :] = sum_{j ascending} w[t, j] * slot_out[slot_of[t*k + j], :]
 // fp32 accumulation in a fixed order (deterministic), one store per element;
 // slot_out in fp32, bf16 or fp16 (both widen exactly).

@@ -1,6 +1,8 @@
-// Top-k routing permutation: per-expert histogram, prefix sum over experts
-// with 128-row aligned segments, and a stable slot assignment (ascending
-// flat index t*k + j within an expert).  Deterministic: counts come from
+// Top-k routing permutation ("NVFP4 MegaMoE Debug Log", Pipeline Trace: the
+// per-expert slot counts of the grouped GEMM; NVFP4 MoE Pipeline, the
+// grouped layout the L1/L2 GEMMs run over): per-expert histogram, prefix sum
+// over experts with 128-row aligned segments, and a stable slot assignment
+// (ascending flat index t*k + j within an expert).  Deterministic: counts come from
 // per-chunk histograms, ranks from warp match + per-warp counts; no global
 // atomics decide any position.
 #include "internal.h"
