@@ -1258,13 +1258,13 @@ __device__ void load_tables(Tables& tb, const GemmArgs& a1, int n_tiles2) {
 
 __device__ uint32_t setup_cta(Barriers* bars, const CUtensorMap* m0, const CUtensorMap* m1,
                               const CUtensorMap* m2, const CUtensorMap* m3,
-                              uint32_t acc_empty_arrivals = 4) {
+                              uint32_t acc_empty_arrivals = 4, uint32_t sf_arrivals = 4) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
-      mbar_init(&bars->sf_full[s], 4);
+      mbar_init(&bars->sf_full[s], sf_arrivals);
     }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, acc_empty_arrivals);
@@ -1855,6 +1855,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
 // Work per CTA before each wait is one or two rounds of 16-element blocks
 // per thread: on a small batch the critical path is a handful of memory
 // round trips, not a loop over whole rows.
+// Warp roles of the layer kernel (7 warps): warp 0 scale writer (see
+// below), warp 1 MMA issuer and TMEM owner, warps 2-5 epilogue, warp 6 TMA
+// producer.  When no tile has a valid row outside TMEM lane quarter 0 (at
+// most 32 rows per expert, e.g. one token), the stage's block scales reach
+// the MMA through warp 0 alone (tcgen05.st into lanes 0-31; the other
+// quarters keep stale scales and produce only accumulator rows that are
+// never stored) instead of tcgen05.cp copies in the tensor pipe, where they
+// paced the weight stream at 0.79 us per stage.  7 warps keep two per SMSP,
+// so the kernel keeps its register budget.
+constexpr int kLayerThreads = 224;
+constexpr int kLayerProducerWarp = 6;
+
 struct LayerArgs {
   const __nv_bfloat16* x;     // [T, H]
   const int32_t* topk_ids;    // [T, k]
@@ -1984,7 +1996,7 @@ __device__ void share_done(int* count) {
   if (threadIdx.x == 64) atomicAdd(count, 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) layer_kernel(
+__global__ void __launch_bounds__(kLayerThreads, 1) layer_kernel(
     const __grid_constant__ AMaps map_x, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ AMaps map_h, const __grid_constant__ CUtensorMap map_w2,
     const GemmArgs a1, const GemmArgs a2, const LayerArgs L) {
@@ -2061,7 +2073,10 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     }
   }
   __syncthreads();
-  const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2);
+  // every valid row in lane quarter 0: one scale-writer warp instead of copies
+  bool one_quarter = true;
+  for (int e = 0; e < E; ++e) one_quarter = one_quarter && tb.cnt[e] <= 32;
+  const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2, 4, 1);
   volatile int* abort = &bars->abort;
   const Phase P1 = make_phase(a1, &map_x, &map_w1, tb.prefix1, E);
   const Phase P2 = make_phase(a2, &map_h, &map_w2, tb.prefix2, E);
@@ -2078,7 +2093,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     else if (warp == 0)
       quantise_share<false>(a1.out, S, I, k, s_dry, dq, dsf, 1.0f, nullptr, nullptr, true);
   }
-  if (warp == 0) {
+  if (warp == kLayerProducerWarp) {
     if (lane == 0) {
       const int G = static_cast<int>(gridDim.x);
       const Gate g1{&L.grid_bar[3], G};
@@ -2098,9 +2113,19 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(
 #pragma unroll 1
       for (int ph = 0; ph < 2; ++ph) {
         const Phase P = ph ? P2 : P1;
-        if (!run_mma<false>(P, bars, smem, tmem, pp, abort)) break;
+        if (one_quarter ? !run_mma<true>(P, bars, smem, tmem, pp, abort)
+                        : !run_mma<false>(P, bars, smem, tmem, pp, abort))
+          break;
       }
       mma_drain(bars, a1.status);
+    }
+  } else if (warp == 0) {
+    if (one_quarter) {
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const Phase P = ph ? P2 : P1;
+        if (!run_sf_writer(P, bars, smem, tmem, pp, abort)) break;
+      }
     }
   } else {
     // The weight loads are already going out; meanwhile the epilogue warps
@@ -2267,7 +2292,7 @@ cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& ma
               l.grid_bar, l.ycnt, l.hq, l.hsf, l.gs_h, l.y, l.y_dtype};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kLayerThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
