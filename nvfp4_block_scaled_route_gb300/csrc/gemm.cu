@@ -19,7 +19,7 @@
 //                         loading L2 weights while the L1 tail and the
 //                         requantisation are still running.
 //
-// Warp roles (one CTA per SM):
+// Warp roles (one CTA per SM; the layer kernel's differ, see there):
 //   warp 0      TMA producer (A tile, two 128-row B tiles, staged scales)
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (and, in the
 //               cooperative kernels, the tcgen05.cp scale copies)
@@ -32,10 +32,12 @@
 //               the 12 copies of a 256-K stage take 1.6x the time of its 4
 //               MMAs, and 5 wide (128x256b) copies 0.5x; stores from warps
 //               overlap the MMAs (98 % of the MMA-only rate, measured with
-//               the library's probe).  The cooperative decode kernels are
-//               bound by HBM, not the tensor pipe, and keep the copies and
-//               6 warps (more warps would cap their registers below what
-//               their epilogue and quantisation code use).
+//               the library's probe).  The cooperative decode kernels cannot
+//               take four more warps (that would cap their registers below
+//               what their epilogue and quantisation code use):
+//               fused_ffn_kernel keeps the copies; layer_kernel has one
+//               writer warp for lane quarter 0, used when every valid row
+//               lies there (one-token batches), else the copies.
 //
 // Shared memory per stage (K = 256 elements = 128 bytes per row):
 //   A 128 rows x 128 B (16 KB), B 256 rows x 128 B (32 KB), both in the
