@@ -402,6 +402,40 @@ def test_layer_kernel_matches_oracle(nb, cfg):
     rows_close(g["y"], y64, "y")
 
 
+LAYER_WIDE = syn.MoEConfig("layer_wide", E=4, H=512, I=256, T=64, k=2, routing="uniform")
+
+
+def test_layer_kernel_many_rows_per_expert(nb):
+    """The single kernel with experts of more than 32 rows (every token on
+    experts 0 and 1: 64 rows each), where valid rows lie outside TMEM lane
+    quarter 0 and the kernel stages the scales with tcgen05.cp copies into
+    every quarter: against the oracle and bit for bit against the four
+    calls.  (With at most 32 rows per expert it stages them with its one
+    writer warp; the tiny and layer16 cases cover that.)"""
+    cfg = LAYER_WIDE
+    x = syn.draw_activations(cfg)
+    _, w = syn.draw_routing(cfg)
+    ids = torch.tensor([[0, 1]] * cfg.T, dtype=torch.int32)
+    W1 = torch.stack([syn.draw_weight(cfg, 1, e) for e in range(cfg.E)])
+    W2 = torch.stack([syn.draw_weight(cfg, 2, e) for e in range(cfg.E)])
+    g = run_gpu_layer(nb, cfg, x, ids, w, W1.to(DEV), W2.to(DEV))
+    b = run_gpu(nb, cfg, x, ids, w, W1.to(DEV), W2.to(DEV), path=1)
+    assert np.array_equal(g["y"], b["y"])
+    w2q = omoe.quantize_expert_weights(list(W2.numpy()))
+    ref = omoe.forward(x.float().numpy(), ids.numpy(), w.numpy(),
+                       *omoe.quantize_expert_weights(list(W1.numpy())), *w2q)
+    r = ref["route"]
+    dense_rows = np.empty(cfg.T * cfg.k, dtype=np.int64)
+    dense_rows[r["slot_of"]] = g["row_of"]
+    rows_close(g["h"][dense_rows], ref["h"], "h")
+    hsf_g = unstage(g["hsf_mma"], g["rows"], cfg.I)[dense_rows]
+    flips = check_requant(ref["h"], ref["gs_h"], ref["hq"], ref["hsf"], g["hq"][dense_rows], hsf_g)
+    y64 = ref["y64"]
+    if sum(flips):
+        _, y64 = flip_adjusted(ref, g["hq"][dense_rows], hsf_g, w2q, w.numpy())
+    rows_close(g["y"], y64, "y")
+
+
 @pytest.mark.parametrize("cfg", [syn.CONFIGS["tiny"], LAYER_SMALL], ids=["tiny", "layer16"])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_layer_kernel_equals_four_calls(nb, cfg, out_dtype):
