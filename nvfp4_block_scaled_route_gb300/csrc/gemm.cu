@@ -75,7 +75,7 @@ constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemBytes = kSmemUsed + 1024;            // alignment slack
-constexpr int kThreads = 192;                           // cooperative kernels
+constexpr int kThreads = 224;                           // cooperative kernels (7 warps)
 constexpr int kThreadsSt = 320;                         // grouped_gemm_kernel<false>
 constexpr int kThreadsHalf = 448;                       // grouped_gemm_kernel<true>
 constexpr int kSfWarp0 = 6;                             // first scale-writer warp
@@ -1757,6 +1757,8 @@ __device__ void requantise(const GemmArgs& a1, const FusedArgs& f, const Tables&
   }
 }
 
+// Like the layer kernel: 7 warps (warp 0 scale writer for one-token
+// batches, warp 1 MMA, warps 2-5 epilogue, warp 6 TMA producer).
 __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
     const __grid_constant__ AMaps map_x, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ AMaps map_h, const __grid_constant__ CUtensorMap map_w2,
@@ -1769,14 +1771,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
   __shared__ int s_last, s_ok;
 
   load_tables(tb, a1, a2.n_tiles);
-  const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2);
+  const uint32_t tmem = setup_cta(bars, &map_x.full, &map_w1, &map_h.full, &map_w2, 4, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars->abort;
   const int E = a1.E;
   const Phase P1 = make_phase(a1, &map_x, &map_w1, tb.prefix1, E);
   const Phase P2 = make_phase(a2, &map_h, &map_w2, tb.prefix2, E);
+  // every valid row in lane quarter 0: one scale-writer warp instead of copies
+  bool one_quarter = true;
+  for (int e = 0; e < E; ++e) one_quarter = one_quarter && tb.cnt[e] <= 32;
   Pipe pp;
-  if (warp == 0) {
+  if (warp == 6) {
     if (lane == 0) {
       const Gate g2{&f.grid_bar[1], 2};
       // both phases through one copy of the role's code (the loop is not
@@ -1793,9 +1798,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
 #pragma unroll 1
       for (int ph = 0; ph < 2; ++ph) {
         const Phase P = ph ? P2 : P1;
-        if (!run_mma<false>(P, bars, smem, tmem, pp, abort)) break;
+        if (one_quarter ? !run_mma<true>(P, bars, smem, tmem, pp, abort)
+                        : !run_mma<false>(P, bars, smem, tmem, pp, abort))
+          break;
       }
       mma_drain(bars, a1.status);
+    }
+  } else if (warp == 0) {
+    if (one_quarter) {
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const Phase P = ph ? P2 : P1;
+        if (!run_sf_writer(P, bars, smem, tmem, pp, abort)) break;
+      }
     }
   } else {
     float amax = 0.0f;
@@ -1866,7 +1881,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_ffn_kernel(
 // never stored) instead of tcgen05.cp copies in the tensor pipe, where they
 // paced the weight stream at 0.79 us per stage.  7 warps keep two per SMSP,
 // so the kernel keeps its register budget.
-constexpr int kLayerThreads = 224;
 constexpr int kLayerProducerWarp = 6;
 
 struct LayerArgs {
@@ -1998,7 +2012,7 @@ __device__ void share_done(int* count) {
   if (threadIdx.x == 64) atomicAdd(count, 1);
 }
 
-__global__ void __launch_bounds__(kLayerThreads, 1) layer_kernel(
+__global__ void __launch_bounds__(kThreads, 1) layer_kernel(
     const __grid_constant__ AMaps map_x, const __grid_constant__ CUtensorMap map_w1,
     const __grid_constant__ AMaps map_h, const __grid_constant__ CUtensorMap map_w2,
     const GemmArgs a1, const GemmArgs a2, const LayerArgs L) {
@@ -2294,7 +2308,7 @@ cudaError_t launch_layer(const GemmArgs& a1, const GemmArgs& a2, const AMaps& ma
               l.grid_bar, l.ycnt, l.hq, l.hsf, l.gs_h, l.y, l.y_dtype};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kLayerThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
